@@ -1,0 +1,210 @@
+"""Seeded synthetic KV-cache workloads (inputs only).
+
+This module produces the inputs that both the CUDA path and the CPU oracle
+consume: per-stream generator parameters, calibration tokens, evaluation
+tokens and paged block tables.  It holds none of the codec's arithmetic (no
+projection, quantisation, packing or bit allocation): it only draws numbers.
+
+Model shapes follow the KV-cache sizes of the models evaluated on the kvtc page
+("KV Cache Transform Coding for Compact Storage in LLM Inference", section 1
+Problem and section 4 Results: Llama 3.1 8B needs 128 MiB per 1K tokens, i.e.
+32 layers x {K,V} x 8 heads x 128 x 2 bytes per token).  No model weights or
+datasets are used: each (layer, K|V) stream is low-rank plus noise,
+
+    x_t = mu + A z_t + 0.01 eps_t,   A = Q_D[:, :r] diag(sigma) Q_r^T,
+    sigma_i = i^(-p),  z ~ N(0, I_r),  eps ~ N(0, I_D),
+
+with four seeded "outlier" channels multiplied by 10 on K streams where the
+workload asks for them, and every value stored as bf16 (round to nearest
+even from fp32).
+
+Seeds (numpy PCG64 via ``default_rng``):
+  generator parameters  3000 + 2*layer + kv
+  calibration tokens    1000 + 2*layer + kv
+  evaluation tokens     2000 + 2*layer + kv + 100000*request
+  paged block table     4242
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import List, Optional, Tuple
+
+import numpy as np
+
+K_STREAM = 0
+V_STREAM = 1
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    layers: int
+    kv: Tuple[int, ...]          # which of K (0) / V (1) are present
+    heads: int
+    head_dim: int
+    tokens: int                  # tokens per request
+    requests: int
+    rank: int
+    spectrum_p: float
+    outliers: bool               # 4 K channels x10
+    sink: int
+    window: int
+    avg_bits: float              # bit budget per coefficient
+    group: int = 16
+    bmax: int = 8
+    n_calib: int = 4096
+    block_size: int = 0          # >0: paged restore into blocks of this many tokens
+    streamed: bool = False       # layer-by-layer restore on one stream
+
+    @property
+    def D(self) -> int:
+        return self.heads * self.head_dim
+
+    @property
+    def budget_bits(self) -> int:
+        return int(round(self.avg_bits * self.D))
+
+    def streams(self) -> List[Tuple[int, int]]:
+        """(layer, kv) pairs in storage order: layer-major, K before V."""
+        return [(l, kv) for l in range(self.layers) for kv in self.kv]
+
+    def raw_bytes(self) -> int:
+        return len(self.streams()) * self.requests * self.tokens * self.D * 2
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", layers=1, kv=(K_STREAM,), heads=2, head_dim=64,
+                     tokens=256, requests=1, rank=32, spectrum_p=1.0,
+                     outliers=False, sink=4, window=16, avg_bits=2.0),
+    "llama31_8b_8k": Workload("llama31_8b_8k", layers=32, kv=(0, 1), heads=8,
+                              head_dim=128, tokens=8192, requests=1, rank=128,
+                              spectrum_p=1.0, outliers=True, sink=4,
+                              window=128, avg_bits=1.0),
+    "mistral_nemo_12b_32k": Workload("mistral_nemo_12b_32k", layers=40,
+                                     kv=(0, 1), heads=8, head_dim=128,
+                                     tokens=32768, requests=1, rank=128,
+                                     spectrum_p=1.5, outliers=True, sink=4,
+                                     window=128, avg_bits=0.5),
+    "llama33_70b_16k": Workload("llama33_70b_16k", layers=80, kv=(0, 1),
+                                heads=8, head_dim=128, tokens=16384,
+                                requests=1, rank=192, spectrum_p=1.0,
+                                outliers=True, sink=4, window=128,
+                                avg_bits=1.0, streamed=True),
+    "qwen25_7b_paged": Workload("qwen25_7b_paged", layers=28, kv=(0, 1),
+                                heads=4, head_dim=128, tokens=4096,
+                                requests=64, rank=128, spectrum_p=1.0,
+                                outliers=False, sink=4, window=128,
+                                avg_bits=2.0, block_size=16),
+}
+
+
+def params_seed(layer: int, kv: int) -> int:
+    return 3000 + 2 * layer + kv
+
+
+def calib_seed(layer: int, kv: int) -> int:
+    return 1000 + 2 * layer + kv
+
+
+def eval_seed(layer: int, kv: int, request: int = 0) -> int:
+    return 2000 + 2 * layer + kv + 100000 * request
+
+
+BLOCK_TABLE_SEED = 4242
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Store generated values as bf16: fp32, then round to nearest even on
+    the top 16 bits.  Generated values are finite, so no NaN handling."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    rounded = b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))
+    return (rounded >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact value of bf16 bit patterns."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+@dataclasses.dataclass
+class StreamParams:
+    mu: np.ndarray               # [D] fp64
+    A: np.ndarray                # [D][r] fp64
+    outlier_channels: np.ndarray  # int64 channel ids (empty if none)
+
+
+def stream_params(w: Workload, layer: int, kv: int) -> StreamParams:
+    rng = np.random.default_rng(params_seed(layer, kv))
+    D, r = w.D, w.rank
+    mu = rng.standard_normal(D)
+    qd, _ = np.linalg.qr(rng.standard_normal((D, r)))
+    qr_, _ = np.linalg.qr(rng.standard_normal((r, r)))
+    sigma = np.arange(1, r + 1, dtype=np.float64) ** (-w.spectrum_p)
+    A = (qd * sigma) @ qr_.T
+    if w.outliers and kv == K_STREAM:
+        ch = np.sort(rng.choice(D, size=4, replace=False)).astype(np.int64)
+    else:
+        ch = np.zeros(0, dtype=np.int64)
+    return StreamParams(mu, A, ch)
+
+
+def _draw(p: StreamParams, rng: np.random.Generator, n: int) -> np.ndarray:
+    D, r = p.A.shape
+    z = rng.standard_normal((n, r))
+    eps = rng.standard_normal((n, D))
+    x = p.mu[None, :] + z @ p.A.T + 0.01 * eps
+    if p.outlier_channels.size:
+        x[:, p.outlier_channels] *= 10.0
+    return f32_to_bf16_bits(x)
+
+
+def calib_tokens(w: Workload, layer: int, kv: int,
+                 params: Optional[StreamParams] = None) -> np.ndarray:
+    """Calibration tokens, bf16 bits [n_calib][D]."""
+    p = params if params is not None else stream_params(w, layer, kv)
+    return _draw(p, np.random.default_rng(calib_seed(layer, kv)), w.n_calib)
+
+
+def eval_tokens(w: Workload, layer: int, kv: int, request: int = 0,
+                T: Optional[int] = None,
+                params: Optional[StreamParams] = None) -> np.ndarray:
+    """Evaluation tokens of one request, bf16 bits [T][D] (numpy)."""
+    p = params if params is not None else stream_params(w, layer, kv)
+    n = w.tokens if T is None else T
+    return _draw(p, np.random.default_rng(eval_seed(layer, kv, request)), n)
+
+
+def eval_tokens_torch(w: Workload, layer: int, kv: int, request: int = 0,
+                      T: Optional[int] = None, device="cuda",
+                      params: Optional[StreamParams] = None):
+    """Same recipe drawn with torch's generator on ``device`` (fast for the
+    multi-GB workloads).  The numbers differ from :func:`eval_tokens` (another
+    generator) but the distribution and seed are the same.  Returns a bf16
+    tensor [T][D]."""
+    import torch
+    p = params if params is not None else stream_params(w, layer, kv)
+    n = w.tokens if T is None else T
+    D, r = p.A.shape
+    g = torch.Generator(device=device)
+    g.manual_seed(eval_seed(layer, kv, request))
+    z = torch.randn((n, r), generator=g, device=device, dtype=torch.float32)
+    eps = torch.randn((n, D), generator=g, device=device, dtype=torch.float32)
+    A = torch.from_numpy(p.A.astype(np.float32)).to(device)
+    mu = torch.from_numpy(p.mu.astype(np.float32)).to(device)
+    x = torch.addmm(mu[None, :], z, A.T)
+    x.add_(eps, alpha=0.01)
+    if p.outlier_channels.size:
+        ch = torch.from_numpy(p.outlier_channels).to(device)
+        x[:, ch] *= 10.0
+    return x.to(torch.bfloat16)
+
+
+def block_table(w: Workload) -> np.ndarray:
+    """Paged layout: a seeded random permutation of all physical blocks,
+    int32 [requests][blocks_per_request]."""
+    assert w.block_size > 0
+    per_req = -(-w.tokens // w.block_size)
+    rng = np.random.default_rng(BLOCK_TABLE_SEED)
+    perm = rng.permutation(w.requests * per_req).astype(np.int32)
+    return perm.reshape(w.requests, per_req)
