@@ -1,0 +1,182 @@
+/*
+ * kvtc.h -- C ABI of the GB300 (sm_103a) KV-cache transform codec.
+ *
+ * The method is KV-cache transform coding ("KV Cache Transform Coding for
+ * Compact Storage in LLM Inference", technical summary section 2):
+ *   compress    (2B)  c = V^T (x - mu), keep the principal components whose
+ *                     group the DP allocation gave a nonzero width, quantise
+ *                     each 16-component group with an fp16 shift and scale
+ *                     of its own (microscaling, 2A), pack the codes;
+ *   decompress  (2C)  unpack, dequantise, x_hat = V c_hat + mu, bf16;
+ *   sinks/window (2A) the first s and the last w tokens are stored raw.
+ * The DEFLATE stage the page runs after packing (2B) is not part of this
+ * library.
+ *
+ * Conventions for every entry point:
+ *   - All device pointers are caller-owned CUDA device memory on the device
+ *     the calibration was loaded on.  The library allocates device memory
+ *     only in kvtc_calib_load (and frees it in kvtc_calib_free); the codec
+ *     calls allocate nothing.
+ *   - Work is enqueued on the caller's stream (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream).  KVTC_OK means "validated
+ *     and enqueued", not "finished".
+ *   - Arguments are validated on the host before any launch; on error
+ *     nothing is enqueued and a negative status is returned.
+ *   - Faults detected by the kernels (fp16 field overflow, a block id out
+ *     of range, a bounded wait that ran out) never trap: the kernel skips
+ *     the affected write and ORs a flag into a sticky per-calibration status
+ *     word, read and cleared with kvtc_device_status.
+ *   - Pointers that the kernels reach with 16-byte vector or bulk copies
+ *     must be 16-byte aligned, and row strides (ld) multiples of 8 elements.
+ *
+ * Formats (all little-endian):
+ *
+ *   Token record (R = 16 * ceil(budget_bits / 128) bytes): for each active
+ *   group g in ascending order a u16 fp16 shift then a u16 fp16 scale; then
+ *   for each active group in ascending order its b_g bit-planes, one u16
+ *   each, bit i of plane j = bit j of the code of the group's i-th
+ *   component; zero padding to R.  Code q of coefficient c:
+ *     shift = fp16 round-down of the group minimum,
+ *     scale = fp16 round-up of (max - shift) / (2^b - 1),
+ *     q = clamp(floor((c - shift) / scale + 1/2), 0, 2^b - 1)  (0 if scale 0),
+ *     c_hat = shift + q * scale.
+ *
+ *   Stream of one (request, layer, K|V) with T tokens, s' = min(s, T),
+ *   w' = min(w, T - s'), T_c = T - s' - w':  s' sink rows (bf16 [s'][D]),
+ *   w' window rows (bf16 [w'][D]), T_c records in token order; the stream
+ *   is padded to a multiple of 256 bytes.  Several streams are concatenated
+ *   in (layer, K, V) order.
+ *
+ *   Calibration blob, version 1: "KVTC", u32 version, n_streams, group (16),
+ *   bmax (8), sink, window, budget_bits; per stream u32 layer, kv (0 = K,
+ *   1 = V), D, k, u8 widths[D/16] zero-padded to a multiple of 8 bytes, f64
+ *   mu[D], f64 V_kept[k][D] (row a = a-th kept principal vector, ascending
+ *   component order), f64 eigenvalues[D]; trailer u32 CRC-32 (IEEE 802.3) of
+ *   all preceding bytes, u32 0.
+ */
+#ifndef KVTC_H
+#define KVTC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum kvtc_status {
+  KVTC_OK = 0,
+  KVTC_EINVAL = -1,   /* null/invalid argument, layer or kv not in blob */
+  KVTC_EFORMAT = -2,  /* blob magic/version/checksum/structure */
+  KVTC_ESIZE = -3,    /* buffer too small, sizes inconsistent */
+  KVTC_ENOMEM = -4,   /* device allocation in kvtc_calib_load failed */
+  KVTC_ECUDA = -5,    /* a CUDA runtime/driver call failed */
+  KVTC_ERANGE = -6,   /* device flag: fp16 field overflow in compress */
+  KVTC_EDEVICE = -7,  /* device flag: bounded wait ran out / bad block id */
+  KVTC_EALIGN = -8,   /* pointer or stride misaligned */
+  KVTC_ENOTSUP = -9   /* shape outside what the kernels support */
+};
+
+/* Sticky device flags reported by kvtc_device_status (bit mask). */
+#define KVTC_FLAG_RANGE 1u     /* a shift/scale left the fp16 range */
+#define KVTC_FLAG_TIMEOUT 2u   /* a bounded mbarrier wait ran out */
+#define KVTC_FLAG_BLOCK 4u     /* block-table id outside [0, num_blocks) */
+
+typedef struct kvtc_calib kvtc_calib;
+
+/*
+ * kvtc_calib_load -- parse a calibration blob and build the device operands.
+ * Reading of technical summary 2A: mu, the basis V and the per-group widths
+ * come from a one-time calibration and are shared by every request.
+ *   blob, blob_bytes : host memory, read only during the call.
+ *   cuda_device      : device ordinal that will run the codec.
+ *   out              : receives an opaque handle (owned by the caller, free
+ *                      with kvtc_calib_free).
+ * Derived on load: bf16 V_kept (projection), fp16 V_kept (reconstruction),
+ * fp32 mu and fp32 m = bf16(V_kept) mu, group layout tables, TMA
+ * descriptors.  Requirements: D % 64 == 0, D <= 8192, k <= 256.
+ * Errors: EINVAL, EFORMAT, ENOMEM, ECUDA, ENOTSUP.
+ */
+int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
+                    kvtc_calib** out);
+void kvtc_calib_free(kvtc_calib* calib);
+
+/* Shape of stream (layer, kv): D, kept components k, sink s, window w,
+ * record bytes R.  Any output pointer may be NULL.  EINVAL if absent. */
+int kvtc_calib_query(const kvtc_calib* calib, int layer, int kv, int* D,
+                     int* k, int* s, int* w, int* record_bytes);
+
+/* Bytes of one stream of T tokens (multiple of 256); < 0 on error. */
+int64_t kvtc_stream_bytes(const kvtc_calib* calib, int layer, int kv,
+                          int64_t T);
+
+/*
+ * kvtc_compress -- technical summary 2B (and 2A for sinks/window).
+ *   layer0, nlayers : layers [layer0, layer0 + nlayers).
+ *   kv_mask         : 1 = K, 2 = V, 3 = both.
+ *   src             : HOST array of 2*nlayers device pointers, entry
+ *                     2*(l - layer0) + kv = bf16 [T][ld] rows of that stream
+ *                     (entries of kinds not in kv_mask are ignored).
+ *   ld              : row stride of src in elements (>= D, % 8 == 0).
+ *   T               : tokens (>= 0).
+ *   dst, dst_bytes  : device output; streams concatenated in (layer, K, V)
+ *                     order, each kvtc_stream_bytes long.
+ * Errors: EINVAL, ESIZE, EALIGN, ECUDA, ENOTSUP.
+ */
+int kvtc_compress(const kvtc_calib* calib, int layer0, int nlayers,
+                  int kv_mask, const void* const* src, int64_t ld, int64_t T,
+                  void* dst, int64_t dst_bytes, void* cuda_stream);
+
+/*
+ * kvtc_decompress -- technical summary 2C.
+ *   src, src_bytes  : device input written by kvtc_compress (same layers,
+ *                     kv_mask and T).
+ *   dst             : HOST array of 2*nlayers device pointers (as src of
+ *                     kvtc_compress), each bf16 [T][ld].
+ *   layer_events    : NULL, or a HOST array of nlayers cudaEvent_t (as
+ *                     void*).  When given, layers are restored one launch
+ *                     per layer in order and event l is recorded once layer
+ *                     layer0 + l is complete, so a consumer can start on
+ *                     early layers (layer-wise decompression, 2C).
+ * Errors: EINVAL, ESIZE, EALIGN, ECUDA, ENOTSUP.
+ */
+int kvtc_decompress(const kvtc_calib* calib, int layer0, int nlayers,
+                    int kv_mask, const void* src, int64_t src_bytes,
+                    int64_t T, void* const* dst, int64_t ld,
+                    void* cuda_stream, void* const* layer_events);
+
+/*
+ * kvtc_decompress_paged -- restore R requests into a paged KV pool (the
+ * block-paged prefix cache of technical summary section 1).
+ *   src          : HOST array [R] of device pointers; src[r] holds request
+ *                  r's streams as kvtc_compress wrote them.
+ *   T            : HOST array [R] of token counts.
+ *   block_table  : DEVICE int32 [R][max_blocks]; token t of request r goes
+ *                  to block block_table[r*max_blocks + t/block_size], row
+ *                  t % block_size.  Ids outside [0, num_blocks) are skipped
+ *                  and flag KVTC_FLAG_BLOCK.
+ *   block_size   : tokens per block (16).
+ *   cache        : HOST array of 2*nlayers device pointers, each bf16
+ *                  [num_blocks][block_size][D] (entries of kinds not in
+ *                  kv_mask ignored).
+ * All selected streams must share one D.  R <= 4096 (split larger sets).
+ * Errors: EINVAL, ESIZE, EALIGN, ECUDA, ENOTSUP.
+ */
+int kvtc_decompress_paged(const kvtc_calib* calib, int layer0, int nlayers,
+                          int kv_mask, const void* const* src,
+                          const int64_t* T, int R, const int32_t* block_table,
+                          int max_blocks, int block_size, void* const* cache,
+                          int64_t num_blocks, void* cuda_stream);
+
+/* Synchronise cuda_stream, then return the sticky device flags in *flags
+ * (KVTC_FLAG_*) and clear them.  Returns KVTC_OK or ECUDA. */
+int kvtc_device_status(const kvtc_calib* calib, void* cuda_stream,
+                       unsigned* flags);
+
+/* Static description of a status code. */
+const char* kvtc_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVTC_H */

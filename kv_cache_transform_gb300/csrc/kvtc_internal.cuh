@@ -1,0 +1,124 @@
+// Internal definitions shared by the host side and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace kvtc {
+
+constexpr int kGroup = 16;         // components per microscaling group
+constexpr int kTileM = 128;        // tokens per tile (MMA M, TMEM lanes)
+constexpr int kAtomK = 64;         // 16-bit elements per 128-byte swizzle row
+constexpr int kMaxK = 256;         // kept components supported
+constexpr int kMaxRecord = 256;    // record bytes supported by the kernels
+constexpr int kMaxD = 8192;
+
+// Device-resident description of one calibrated (layer, K|V) stream; built
+// once by kvtc_calib_load and read by every kernel launch.
+struct DevStream {
+  CUtensorMap tm_vdec;      // fp16 V_kept as [D rows][k cols], box {64, nc}
+  CUtensorMap tm_venc;      // bf16 V_kept as [k rows][D cols], box {64, k}
+  const float* mu;          // [D]   fp32 mean
+  const float* m;           // [k]   fp32 projection of the mean
+  const uint8_t* bits;      // [Ga]  width of each active group
+  const uint16_t* poff;     // [Ga]  byte offset of the group's first plane
+  int32_t D, k, Ga, R;      // R = record bytes
+  int32_t nc;               // reconstruction N chunk: 128 or 64
+  int32_t pad[3];
+};
+
+// ---------------------------------------------------------------- compress
+constexpr int kCompMaxSeg = 64;
+struct CompSeg {
+  CUtensorMap tm_x;         // bf16 rows [s'+T_c][D] of the source, box {64,128}
+  uint8_t* rec;             // first record of the stream (device)
+  int32_t tc;               // compressed tokens
+  int32_t row0;             // s' (first compressed source row)
+  int32_t cs;               // calibration stream index
+  int32_t tile_begin;       // first work item of this segment
+};
+struct CompParams {
+  CompSeg seg[kCompMaxSeg];
+  const DevStream* streams;
+  unsigned* status;
+  int32_t nseg;
+  int32_t total_tiles;
+  int32_t nstages;
+  int32_t stage_bytes;      // A + B bytes of one pipeline stage
+  int32_t b_bytes_max;      // B bytes reserved per stage
+  int32_t rec_stg_words;    // record staging words per thread
+};
+
+// -------------------------------------------------------------- decompress
+constexpr int kDecMaxSeg = 256;
+struct DecSeg {
+  const uint8_t* rec;       // first record
+  char* dst;                // output row of the first compressed token
+  int64_t ld_bytes;         // output row stride
+  int32_t tc;
+  int32_t cs;
+  int32_t tile_begin;
+  int32_t pad;
+};
+struct DecParams {
+  DecSeg seg[kDecMaxSeg];
+  const DevStream* streams;
+  unsigned* status;
+  int32_t nseg;
+  int32_t total_tiles;
+};
+
+// Paged restore: work items are (request, stream, tile).
+constexpr int kPagedMaxReq = 256;
+constexpr int kPagedMaxStream = 256;
+struct PagedParams {
+  const uint8_t* src[kPagedMaxReq];      // request's concatenated streams
+  int64_t sbytes[kPagedMaxReq];          // bytes of one stream of request r
+  int32_t tc[kPagedMaxReq];              // compressed tokens of request r
+  int32_t s_[kPagedMaxReq];              // sink rows kept of request r
+  int32_t raw_rows[kPagedMaxReq];        // s' + w' of request r
+  int32_t tile_begin[kPagedMaxReq + 1];
+  int64_t raw_begin[kPagedMaxReq + 1];   // first raw 16-byte chunk of request r
+  int32_t req_index[kPagedMaxReq];       // absolute request id (block table row)
+  char* cache[kPagedMaxStream];          // pool of stream j
+  int32_t cs[kPagedMaxStream];           // calibration stream of stream j
+  const DevStream* streams;
+  unsigned* status;
+  const int32_t* block_table;
+  int64_t num_blocks;
+  int32_t max_blocks;
+  int32_t block_size;
+  int32_t nreq;
+  int32_t nstream;
+  int32_t total_tiles;
+  int32_t D;
+  int64_t total_raw_chunks;
+};
+
+// ---------------------------------------------------------------- raw rows
+constexpr int kRawMaxSeg = 256;
+struct RawSeg {
+  const char* src;          // source row base
+  char* dst;                // destination row base
+  int64_t src_ld, dst_ld;   // row strides in bytes
+  int32_t rows;             // rows to copy
+  int32_t row_bytes;        // bytes per row (multiple of 16)
+  int64_t chunk_begin;      // first 16-byte chunk index of this segment
+};
+struct RawParams {
+  RawSeg seg[kRawMaxSeg];
+  int32_t nseg;
+  int64_t total_chunks;
+};
+
+// Launchers (kvtc_kernels.cu).  Return a cudaError_t.
+cudaError_t launch_compress(const CompParams& p, int grid, cudaStream_t st);
+cudaError_t launch_decompress(const DecParams& p, int grid, cudaStream_t st);
+cudaError_t launch_decompress_paged(const PagedParams& p, int grid,
+                                    cudaStream_t st);
+cudaError_t launch_raw_copy(const RawParams& p, cudaStream_t st);
+cudaError_t launch_paged_raw(const PagedParams& p, cudaStream_t st);
+int compress_smem_bytes(int nstages, int stage_bytes, int rec_stg_words);
+int decompress_smem_bytes();
+
+}  // namespace kvtc

@@ -1,0 +1,269 @@
+"""CUDA path vs the fp64 oracle, through the C ABI (needs a GB300)."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import codec, fp
+
+from _parity import (blob_for, calibrate_workload, check_decompress,
+                     check_records, stream_calibs)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kv():
+    from kv_cache_transform_gb300 import _build
+    _build.build()
+    import kv_cache_transform_gb300 as kv
+    return kv
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch
+    assert torch.cuda.is_available()
+    return torch
+
+
+def to_dev(torch, bits: np.ndarray, ld: int = None):
+    T, D = bits.shape
+    ld = ld or D
+    t = torch.zeros((T, ld), dtype=torch.int16, device="cuda")
+    if T:
+        t[:, :D] = torch.from_numpy(bits.view(np.int16).copy()).cuda()
+    return t
+
+
+def from_dev(t) -> np.ndarray:
+    return t.cpu().numpy().view(np.uint16)
+
+
+def run_roundtrip(kv, torch, name, streams, T, ld_pad=0, sample=None):
+    """Compress x of each stream on the GPU and with the oracle, compare;
+    decompress the oracle's bitstream on the GPU, compare."""
+    w = synth.WORKLOADS[name]
+    entries = calibrate_workload(name, streams)
+    blob = blob_for(name, entries)
+    scs = stream_calibs(blob)
+    calib = kv.kvtc_calib_load(blob, 0)
+    layers = sorted({l for l, _ in streams})
+    layer0, nl = layers[0], layers[-1] - layers[0] + 1
+    kinds = sorted({k for _, k in streams})
+    mask = sum(1 << k for k in kinds)
+    D = w.D
+    ld = D + ld_pad
+    xs, src = {}, [None] * (2 * nl)
+    for l, k in streams:
+        xs[(l, k)] = synth.eval_tokens(w, l, k, T=T)
+        src[2 * (l - layer0) + k] = to_dev(torch, xs[(l, k)], ld)
+    order = [(l, k) for l in range(layer0, layer0 + nl) for k in kinds]
+    sizes = [calib.stream_bytes(l, k, T) for l, k in order]
+    total = sum(sizes)
+    dst = torch.full((max(total, 16),), -1, dtype=torch.uint8, device="cuda")
+    kv.kvtc_compress(calib, layer0, nl, mask, src, ld, T, dst, total)
+    assert kv.kvtc_device_status(calib) == 0
+    gpu = dst.cpu().numpy()[:total]
+    s_, w_, tc = codec.split_tokens(T, w.sink, w.window)
+    off = 0
+    oracle_stream = {}
+    stats = []
+    for (l, k), sz in zip(order, sizes):
+        sc_enc, sc_dec = scs[(l, k)]
+        g = gpu[off:off + sz].tobytes()
+        o = codec.compress_stream(xs[(l, k)], sc_enc)
+        assert len(o) == sz
+        raw = (s_ + w_) * D * 2
+        assert g[:raw] == o[:raw], "raw rows differ"
+        R = sc_enc.R
+        assert g[raw + tc * R:] == o[raw + tc * R:], "padding differs"
+        rows = np.arange(tc) if sample is None else sample(tc)
+        grec = np.frombuffer(g, np.uint8, tc * R, raw).reshape(tc, R)[rows]
+        st = check_records(grec, xs[(l, k)][s_ + rows], sc_enc)
+        assert st["bad"] == 0, st
+        stats.append(st)
+        oracle_stream[(l, k)] = o
+        off += sz
+    # decompress the oracle's bitstream
+    ob = b"".join(oracle_stream[s] for s in order)
+    srcd = torch.from_numpy(np.frombuffer(ob, np.uint8).copy()).cuda() \
+        if ob else torch.zeros(16, dtype=torch.uint8, device="cuda")
+    outs = [None] * (2 * nl)
+    for l, k in streams:
+        outs[2 * (l - layer0) + k] = torch.full((max(T, 1), ld), 0x7FC0,
+                                                dtype=torch.int16,
+                                                device="cuda")
+    kv.kvtc_decompress(calib, layer0, nl, mask, srcd, len(ob), T, outs, ld)
+    assert kv.kvtc_device_status(calib) == 0
+    dstats = []
+    for l, k in streams:
+        sc_enc, sc_dec = scs[(l, k)]
+        got = from_dev(outs[2 * (l - layer0) + k])[:T, :D]
+        ref = codec.decompress_stream(oracle_stream[(l, k)], T, sc_dec)
+        np.testing.assert_array_equal(got[:s_], ref[:s_])
+        np.testing.assert_array_equal(got[T - w_:], ref[T - w_:])
+        st = check_decompress(got[s_:T - w_], ref[s_:T - w_])
+        assert st["ok"], st
+        dstats.append(st)
+        if ld_pad:  # padding columns untouched
+            pad = from_dev(outs[2 * (l - layer0) + k])[:T, D:]
+            assert np.all(pad == 0x7FC0)
+    calib.free()
+    return stats, dstats
+
+
+@pytest.mark.parametrize("T", [0, 1, 4, 20, 21, 147, 256, 1000, 2049])
+def test_tiny_parity(kv, torch, T):
+    run_roundtrip(kv, torch, "tiny", [(0, 0)], T)
+
+
+def test_tiny_row_stride(kv, torch):
+    run_roundtrip(kv, torch, "tiny", [(0, 0)], 700, ld_pad=24)
+
+
+def test_llama_shape_several_streams_ragged(kv, torch):
+    stats, dstats = run_roundtrip(
+        kv, torch, "llama31_8b_8k", [(3, 0), (3, 1), (4, 0), (4, 1)], 1000)
+    print(stats, dstats)
+
+
+def test_nemo_shape_k112(kv, torch):
+    run_roundtrip(kv, torch, "mistral_nemo_12b_32k", [(0, 0), (0, 1)], 1500)
+
+
+def test_paged_restore_and_block_flag(kv, torch):
+    name = "qwen25_7b_paged"
+    w = synth.WORKLOADS[name]
+    streams = [(0, 0), (0, 1), (1, 0), (1, 1)]
+    entries = calibrate_workload(name, streams)
+    blob = blob_for(name, entries)
+    scs = stream_calibs(blob)
+    calib = kv.kvtc_calib_load(blob, 0)
+    Ts = [700, 37, 4096, 129]
+    bs = 16
+    maxb = -(-max(Ts) // bs)
+    nblocks = len(Ts) * maxb + 7
+    rng = np.random.default_rng(5)
+    table = rng.permutation(nblocks)[:len(Ts) * maxb].astype(np.int32)
+    table = table.reshape(len(Ts), maxb)
+    D = w.D
+    srcs, oracle_bytes = [], []
+    for r, T in enumerate(Ts):
+        parts = []
+        for l, k in streams:
+            x = synth.eval_tokens(w, l, k, request=r, T=T)
+            parts.append(codec.compress_stream(x, scs[(l, k)][0]))
+        b = b"".join(parts)
+        oracle_bytes.append(parts)
+        srcs.append(torch.from_numpy(np.frombuffer(b, np.uint8).copy()).cuda())
+    caches = [torch.full((nblocks, bs, D), 0x7FC0, dtype=torch.int16,
+                         device="cuda") for _ in range(4)]
+    bt = torch.from_numpy(table).cuda()
+    kv.kvtc_decompress_paged(calib, 0, 2, 3, srcs, Ts, bt, maxb, bs, caches,
+                             nblocks)
+    assert kv.kvtc_device_status(calib) == 0
+    host = [from_dev(c) for c in caches]
+    for r, T in enumerate(Ts):
+        s_, w_, tc = codec.split_tokens(T, w.sink, w.window)
+        for j, (l, k) in enumerate(streams):
+            ref = codec.decompress_stream(oracle_bytes[r][j], T, scs[(l, k)][1])
+            t = np.arange(T)
+            got = host[j][table[r, t // bs], t % bs]
+            np.testing.assert_array_equal(got[:s_], ref[:s_])
+            np.testing.assert_array_equal(got[T - w_:], ref[T - w_:])
+            st = check_decompress(got[s_:T - w_], ref[s_:T - w_])
+            assert st["ok"], st
+    # untouched blocks keep their contents
+    used = set(table[r, t] for r, T in enumerate(Ts)
+               for t in range(-(-T // bs)))
+    free = [b for b in range(nblocks) if b not in used]
+    for c in host:
+        assert np.all(c[free] == 0x7FC0)
+    # an out-of-range block id is skipped and flagged, not a fault
+    bad = table.copy()
+    bad[2, 5] = nblocks + 3
+    bad[3, 0] = -1
+    kv.kvtc_decompress_paged(calib, 0, 2, 3, srcs, Ts,
+                             torch.from_numpy(bad).cuda(), maxb, bs, caches,
+                             nblocks)
+    assert kv.kvtc_device_status(calib) & kv.KVTC_FLAG_BLOCK
+    assert kv.kvtc_device_status(calib) == 0  # cleared after reading
+    calib.free()
+
+
+def test_layer_events_match_single_launch(kv, torch):
+    name = "llama31_8b_8k"
+    w = synth.WORKLOADS[name]
+    streams = [(l, k) for l in range(3) for k in (0, 1)]
+    entries = calibrate_workload(name, streams)
+    blob = blob_for(name, entries)
+    calib = kv.kvtc_calib_load(blob, 0)
+    T = 600
+    src = [to_dev(torch, synth.eval_tokens(w, l, k, T=T)) for l, k in streams]
+    total = sum(calib.stream_bytes(l, k, T) for l, k in streams)
+    comp = torch.zeros(total, dtype=torch.uint8, device="cuda")
+    kv.kvtc_compress(calib, 0, 3, 3, src, w.D, T, comp, total)
+    a = [torch.zeros((T, w.D), dtype=torch.int16, device="cuda")
+         for _ in streams]
+    b = [torch.zeros((T, w.D), dtype=torch.int16, device="cuda")
+         for _ in streams]
+    kv.kvtc_decompress(calib, 0, 3, 3, comp, total, T, a, w.D)
+    evs = [torch.cuda.Event() for _ in range(3)]
+    for e in evs:  # torch creates the CUDA event on its first record
+        e.record()
+    kv.kvtc_decompress(calib, 0, 3, 3, comp, total, T, b, w.D,
+                       layer_events=evs)
+    evs[0].synchronize()
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    assert kv.kvtc_device_status(calib) == 0
+    calib.free()
+
+
+def test_full_llama31_8b_8k_sampled(kv, torch):
+    """Full workload as the bench launches it (64 streams x 8192 tokens, one
+    call each way); eight streams are checked against the oracle in full."""
+    name = "llama31_8b_8k"
+    w = synth.WORKLOADS[name]
+    streams = w.streams()
+    entries = calibrate_workload(name, streams)
+    blob = blob_for(name, entries)
+    scs = stream_calibs(blob)
+    calib = kv.kvtc_calib_load(blob, 0)
+    T, D = w.tokens, w.D
+    src = [synth.eval_tokens_torch(w, l, k, T=T).view(torch.int16)
+           for l, k in streams]
+    total = sum(calib.stream_bytes(l, k, T) for l, k in streams)
+    comp = torch.zeros(total, dtype=torch.uint8, device="cuda")
+    kv.kvtc_compress(calib, 0, w.layers, 3, src, D, T, comp, total)
+    outs = [torch.zeros((T, D), dtype=torch.int16, device="cuda")
+            for _ in streams]
+    kv.kvtc_decompress(calib, 0, w.layers, 3, comp, total, T, outs, D)
+    assert kv.kvtc_device_status(calib) == 0
+    sb = calib.stream_bytes(0, 0, T)
+    s_, w_, tc = codec.split_tokens(T, w.sink, w.window)
+    raw = (s_ + w_) * D * 2
+    gbytes = comp.cpu().numpy()
+    worst = 0.0
+    for idx in (0, 1, 14, 27, 40, 51, 62, 63):
+        l, k = streams[idx]
+        sc_enc, sc_dec = scs[(l, k)]
+        x = from_dev(src[idx])
+        g = gbytes[idx * sb:(idx + 1) * sb].tobytes()
+        o = codec.compress_stream(x, sc_enc)
+        assert g[:raw] == o[:raw]
+        grec = np.frombuffer(g, np.uint8, tc * sc_enc.R, raw).reshape(
+            tc, sc_enc.R)
+        st = check_records(grec, x[s_:T - w_], sc_enc)
+        assert st["bad"] == 0, (idx, st)
+        # GPU decompress of the GPU bitstream vs the oracle decompressing
+        # the same bitstream
+        ref = codec.decompress_stream(g, T, sc_dec)
+        got = from_dev(outs[idx])
+        np.testing.assert_array_equal(got[:s_], x[:s_])
+        np.testing.assert_array_equal(got[T - w_:], x[T - w_:])
+        dst = check_decompress(got[s_:T - w_], ref[s_:T - w_])
+        assert dst["ok"], (idx, dst)
+        worst = max(worst, dst["rel_l2"])
+    calib.free()
