@@ -1,0 +1,426 @@
+"""Throughput of the kvtc hot path on GB300 (one JSON line on stdout).
+
+A step is one pass of the whole path over the workload: compress every
+(layer, K|V) stream of the Llama-3.1-8B-shaped 8K-token KV cache (sink and
+window rows raw, tensor-core projection, microscaled quantisation, bit-plane
+packing), then restore all of it (unpack, dequantise, tensor-core
+reconstruction, bf16 rows).  Calibration (mean, basis, widths) runs once,
+before the timed region, with the library's own GPU calibration.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun, one rank per GPU, each restoring its own copy
+of the workload (weak scaling; the streams are independent, no collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = ("restored-KV GB/s (decompress) & compress GB/s at 1 GB300; "
+          "% of roofline")
+WORKLOAD = "llama31_8b_8k"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                  "bf16_tflops_sustained": 1700.0}
+# DRAM bytes per launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum)
+# of the kernel as it is now, per launch of the bench workload; None when the
+# kernel has changed since the capture.
+NCU_TRAFFIC = {"decompress": None, "compress": None}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def workload_desc(w):
+    return (f"{w.name}: {w.layers} layers x {{K,V}}, {w.heads}x{w.head_dim} "
+            f"(D={w.D}), {w.tokens} tokens bf16, {w.avg_bits:g} bit/coef "
+            f"budget, sink {w.sink}, window {w.window}, groups of {w.group}")
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# --------------------------------------------------------------- oracle arm
+def oracle_sample(w, n_streams: int, T: int):
+    """Oracle compress + decompress of a bounded sample of streams; returns
+    (seconds per stream-pass, restored bytes per stream-pass, threads)."""
+    from oracle import calibrate, codec
+    entries = []
+    for l, k in w.streams()[:n_streams]:
+        cb = synth.calib_tokens(w, l, k)
+        mu, V, ev, widths, _ = calibrate.calibrate_stream(cb, w.budget_bits)
+        entries.append((l, k, mu, V, ev, widths))
+    blob = calibrate.write_blob(entries, w.sink, w.window, w.budget_bits)
+    b = calibrate.read_blob(blob)
+    xs = [synth.eval_tokens(w, l, k, T=T) for l, k in w.streams()[:n_streams]]
+    t0 = time.perf_counter()
+    for e, x in zip(b["streams"], xs):
+        sc_e = calibrate.stream_calib(e, w.sink, w.window, w.budget_bits,
+                                      "bf16")
+        sc_d = calibrate.stream_calib(e, w.sink, w.window, w.budget_bits,
+                                      "fp16")
+        buf = codec.compress_stream(x, sc_e)
+        codec.decompress_stream(buf, T, sc_d)
+    dt = time.perf_counter() - t0
+    return dt, n_streams * T * w.D * 2, os.cpu_count()
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[args.workload]
+    T = w.tokens
+    times = []
+    for _ in range(args.warmup):
+        oracle_sample(w, 1, T)
+    nbytes = 0
+    cores = os.cpu_count()
+    for _ in range(args.steps):
+        dt, nbytes, cores = oracle_sample(w, 1, T)
+        times.append(dt)
+    total = sum(times)
+    value = args.steps * nbytes / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": workload_desc(w)},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"per step: oracle compress + decompress "
+                                   f"of 1 of {len(w.streams())} streams "
+                                   f"({T} tokens x D={w.D}), restored bytes "
+                                   f"per second"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import torch
+    import kv_cache_transform_gb300 as kv
+    from kv_cache_transform_gb300 import _build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    kv.lib()
+    w = synth.WORKLOADS[args.workload]
+    streams = w.streams()
+    T, D = w.tokens, w.D
+    stream = torch.cuda.current_stream()
+
+    # one-time calibration on the GPU (not timed)
+    t0 = time.perf_counter()
+    cal = [synth.calib_tokens_torch(w, l, k) for l, k in streams]
+    blob = kv.kvtc_calibrate(cal, [l for l, _ in streams],
+                             [k for _, k in streams], w.n_calib, D, D,
+                             w.sink, w.window, w.budget_bits, device=dev)
+    del cal
+    calib = kv.kvtc_calib_load(blob, dev)
+    calib_s = time.perf_counter() - t0
+    ks = sorted({calib.query(l, k)["k"] for l, k in streams})
+
+    x = [synth.eval_tokens_torch(w, l, k, T=T) for l, k in streams]
+    total = sum(calib.stream_bytes(l, k, T) for l, k in streams)
+    comp = torch.empty(total, dtype=torch.uint8, device="cuda")
+    out = [torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+           for _ in streams]
+
+    def compress():
+        kv.kvtc_compress(calib, 0, w.layers, 3, x, D, T, comp, total, stream)
+
+    def decompress():
+        kv.kvtc_decompress(calib, 0, w.layers, 3, comp, total, T, out, D,
+                           stream)
+
+    for _ in range(max(3, args.warmup)):
+        compress()
+        decompress()
+    torch.cuda.synchronize()
+    flags = kv.kvtc_device_status(calib)
+    if flags:
+        raise RuntimeError(f"device flags {flags} after warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+          for _ in range(args.steps)]
+    launches0 = kv.kvtc_launch_count()
+    with ClockSampler(dev) as clocks:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            compress()
+            ev[i][1].record(stream)
+            decompress()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    launches = kv.kvtc_launch_count() - launches0
+    t_comp = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    t_dec = sum(e[1].elapsed_time(e[2]) for e in ev) / 1e3
+    t_step = sum(e[0].elapsed_time(e[2]) for e in ev) / 1e3
+    if world > 1:
+        t = torch.tensor([t_comp, t_dec, t_step], device="cuda",
+                         dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_comp, t_dec, t_step = (float(v) for v in t.tolist())
+    flags = kv.kvtc_device_status(calib)
+
+    # algorithmic bytes and FLOPs of one pass (per direction)
+    s_ = min(w.sink, T)
+    w_ = min(w.window, T - s_)
+    tc = T - s_ - w_
+    raw_kv = len(streams) * T * D * 2
+    rec = sum(tc * calib.query(l, k)["record_bytes"] for l, k in streams)
+    raw_rows = len(streams) * (s_ + w_) * D * 2
+    dec_bytes = rec + raw_rows + raw_kv          # records + raw in, all out
+    comp_bytes = raw_kv + rec + raw_rows         # all in, records + raw out
+    flops = sum(2 * D * calib.query(l, k)["k"] * tc for l, k in streams)
+    peaks, peak_kind = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    tflops = float(peaks["bf16_tflops"])
+
+    def roof(nbytes, t, name):
+        t_mem = nbytes / (hbm * 1e9)
+        t_mma = flops / (tflops * 1e12)
+        per = t / args.steps
+        if t_mem >= t_mma:
+            ach = nbytes / per / 1e9
+            r = {"bound": "hbm", "achieved": ach, "peak": hbm,
+                 "unit": "GB/s", "frac": ach / hbm}
+        else:
+            ach = flops / per / 1e12
+            r = {"bound": "tensor", "achieved": ach, "peak": tflops,
+                 "unit": "TFLOP/s", "frac": ach / tflops}
+        r.update({"traffic": NCU_TRAFFIC[name], "kernel": name,
+                  "algorithmic_bytes": nbytes, "flops": flops,
+                  "t_roof_us": 1e6 * max(t_mem, t_mma),
+                  "frac_of_roofline": 1e6 * max(t_mem, t_mma) / (1e6 * per),
+                  "peak_source": f"{peak_kind} (MEASURED_PEAKS.json burst)"
+                  if peak_kind == "measured" else "fallback"})
+        return r
+
+    roof_dec = roof(dec_bytes, t_dec, "decompress")
+    roof_comp = roof(comp_bytes, t_comp, "compress")
+    dominant = roof_dec if t_dec >= t_comp else roof_comp
+
+    # end to end through the public API with host buffers: compressed
+    # streams in pinned host memory -> device -> restore; the status word
+    # (the step's result flag) read back; and the compress direction with
+    # raw KV from pinned host memory and the streams read back.
+    e2e = run_e2e(kv, torch, calib, w, comp, out, x, total, stream,
+                  max(3, args.steps // 2))
+
+    line = {
+        "metric": METRIC,
+        "value": world * raw_kv * args.steps / t_dec / 1e9,
+        "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t_step / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(w), "streams": len(streams),
+                   "tokens": T, "D": D, "k": ks,
+                   "record_bytes": calib.query(0, 0)["record_bytes"],
+                   "l2": "inputs larger than L2: 1.07 GB per direction",
+                   "calibration_s": round(calib_s, 2)},
+        "compress": {"value": world * raw_kv * args.steps / t_comp / 1e9,
+                     "unit": "GB/s", "ms": 1e3 * t_comp / args.steps,
+                     "compressed_out_gbs": world * (rec + raw_rows) *
+                     args.steps / t_comp / 1e9},
+        "decompress": {"value": world * raw_kv * args.steps / t_dec / 1e9,
+                       "unit": "GB/s", "ms": 1e3 * t_dec / args.steps,
+                       "compressed_in_gbs": world * (rec + raw_rows) *
+                       args.steps / t_dec / 1e9},
+        "compression_ratio": raw_kv / total,
+        "roofline": dominant,
+        "rooflines": {"decompress": roof_dec, "compress": roof_comp},
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+        "device_flags": flags,
+    }
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            dt, nb, cores = oracle_sample(w, 1, T)
+            line["cpu_baseline"] = {
+                "value": nb / dt / 1e9, "unit": "GB/s", "cores": cores,
+                "kind": "oracle",
+                "sample": f"oracle compress + decompress of 1 of "
+                          f"{len(streams)} streams ({T} tokens x D={D}); "
+                          f"restored bytes per second"}
+        print(json.dumps(line), flush=True)
+    calib.free()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(kv, torch, calib, w, comp, out, x, total, stream, steps):
+    T, D = w.tokens, w.D
+    host_comp = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    host_comp.copy_(comp)
+    dev_comp = torch.empty_like(comp)
+    flags = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    raw_kv = len(x) * T * D * 2
+    torch.cuda.synchronize()
+    # decompress direction
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        dev_comp.copy_(host_comp, non_blocking=True)
+        kv.kvtc_decompress(calib, 0, w.layers, 3, dev_comp, total, T, out, D,
+                           stream)
+        kv.kvtc_device_status(calib, stream)  # syncs, reads the flags back
+    b.record(stream)
+    torch.cuda.synchronize()
+    t_dec = a.elapsed_time(b) / 1e3
+    # compress direction
+    host_x = [torch.empty((T, D), dtype=torch.bfloat16, pin_memory=True)
+              for _ in x]
+    for h, d in zip(host_x, x):
+        h.copy_(d)
+    dev_x = [torch.empty_like(d) for d in x]
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(steps):
+        for h, d in zip(host_x, dev_x):
+            d.copy_(h, non_blocking=True)
+        kv.kvtc_compress(calib, 0, w.layers, 3, dev_x, D, T, dev_comp, total,
+                         stream)
+        host_comp.copy_(dev_comp, non_blocking=True)
+    b.record(stream)
+    torch.cuda.synchronize()
+    t_comp = a.elapsed_time(b) / 1e3
+    del flags
+    return {"value": raw_kv * steps / t_dec / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": total, "d2h_bytes_per_step": 4,
+            "what": "restore: compressed streams H2D from pinned memory, "
+                    "kvtc_decompress into device KV, status word read back",
+            "compress": {"value": raw_kv * steps / t_comp / 1e9,
+                         "unit": "GB/s", "h2d_bytes_per_step": raw_kv,
+                         "d2h_bytes_per_step": total}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=sorted(k for k, v in synth.WORKLOADS.items()
+                                   if v.requests == 1))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -168,10 +168,41 @@ int kvtc_decompress_paged(const kvtc_calib* calib, int layer0, int nlayers,
                           int max_blocks, int block_size, void* const* cache,
                           int64_t num_blocks, void* cuda_stream);
 
+/*
+ * kvtc_calibrate -- the one-time calibration of technical summary 2A, on
+ * the GPU, writing a version-1 blob (format above).  Per stream: mu = mean of
+ * the calibration rows; V = eigenvectors of their covariance, sorted by
+ * eigenvalue descending, each signed so that its largest-magnitude entry is
+ * positive; E[g][b] = summed squared coefficient error of group g at width
+ * b (b = 0: the group's energy) measured with the codec's quantiser; widths
+ * = the DP allocation minimising sum E[g][b_g] with sum (32 + 16 b_g) over
+ * groups with b_g > 0 at most budget_bits (ties keep the smaller width).
+ *   tokens      : HOST array [n] of device pointers, stream i's calibration
+ *                 rows, bf16 [N][ld]; layers, kvs: HOST arrays [n].
+ *   blob        : HOST output of capacity bytes (kvtc_blob_max_bytes is an
+ *                 upper bound); *blob_bytes receives the size (also when
+ *                 the capacity is too small: ESIZE).
+ * Unlike the codec calls it allocates temporary device memory (freed before
+ * returning) and synchronises cuda_stream.  fp64 arithmetic; covariance and
+ * coefficient products use cuBLAS, the eigensolver cuSOLVER.
+ * Errors: EINVAL, ENOMEM, ECUDA, ESIZE.
+ */
+int kvtc_calibrate(int cuda_device, int n, const int* layers, const int* kvs,
+                   const void* const* tokens, int64_t N, int64_t ld, int D,
+                   int sink, int window, int budget_bits, void* blob,
+                   size_t capacity, size_t* blob_bytes, void* cuda_stream);
+
+/* Upper bound on the blob size of n streams of width D (< 0 on error). */
+int64_t kvtc_blob_max_bytes(int n, int D);
+
 /* Synchronise cuda_stream, then return the sticky device flags in *flags
  * (KVTC_FLAG_*) and clear them.  Returns KVTC_OK or ECUDA. */
 int kvtc_device_status(const kvtc_calib* calib, void* cuda_stream,
                        unsigned* flags);
+
+/* Number of kernels this library has launched since it was loaded (all
+ * devices and threads); a cheap way for callers to count launches. */
+uint64_t kvtc_launch_count(void);
 
 /* Static description of a status code. */
 const char* kvtc_strerror(int status);

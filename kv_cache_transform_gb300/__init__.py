@@ -6,7 +6,7 @@ mirror the C ABI in ``include/kvtc.h``:
 
     kvtc_calib_load, kvtc_calib_free, kvtc_calib_query, kvtc_stream_bytes,
     kvtc_compress, kvtc_decompress, kvtc_decompress_paged,
-    kvtc_device_status, kvtc_strerror
+    kvtc_device_status, kvtc_launch_count, kvtc_strerror
 
 Tensor arguments are torch CUDA tensors (or raw integer device addresses);
 ``stream`` defaults to torch's current stream.  There is no CPU fallback: if
@@ -75,6 +75,11 @@ def lib() -> ctypes.CDLL:
         "kvtc_device_status": (c_i, [c_vp, c_vp,
                                      ctypes.POINTER(ctypes.c_uint)]),
         "kvtc_strerror": (ctypes.c_char_p, [c_i]),
+        "kvtc_calibrate": (c_i, [c_i, c_i, c_ip, c_ip, c_pp, c_i64, c_i64,
+                                 c_i, c_i, c_i, c_i, c_vp, c_sz,
+                                 ctypes.POINTER(ctypes.c_size_t), c_vp]),
+        "kvtc_blob_max_bytes": (c_i64, [c_i, c_i]),
+        "kvtc_launch_count": (ctypes.c_uint64, []),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -82,6 +87,10 @@ def lib() -> ctypes.CDLL:
         f.argtypes = args
     _lib_handle = L
     return L
+
+
+def kvtc_launch_count() -> int:
+    return int(lib().kvtc_launch_count())
 
 
 def kvtc_strerror(code: int) -> str:
@@ -155,6 +164,28 @@ def kvtc_calib_load(blob: bytes, device: int = 0) -> Calib:
     _check(lib().kvtc_calib_load(buf, len(blob), device, ctypes.byref(out)),
            "kvtc_calib_load")
     return Calib(out.value, device)
+
+
+def kvtc_calibrate(tokens: Sequence, layers: Sequence[int],
+                   kvs: Sequence[int], N: int, ld: int, D: int, sink: int,
+                   window: int, budget_bits: int, device: int = 0,
+                   stream=None) -> bytes:
+    """Calibrate streams from device bf16 rows [N][ld]; returns the blob."""
+    n = len(tokens)
+    cap = _check(lib().kvtc_blob_max_bytes(n, D), "kvtc_blob_max_bytes")
+    buf = ctypes.create_string_buffer(cap)
+    size = ctypes.c_size_t()
+    L = (ctypes.c_int * n)(*layers)
+    K = (ctypes.c_int * n)(*kvs)
+    _check(lib().kvtc_calibrate(device, n, L, K, _ptr_array(tokens), N, ld,
+                                D, sink, window, budget_bits, buf, cap,
+                                ctypes.byref(size), _stream(stream) or None),
+           "kvtc_calibrate")
+    return buf.raw[:size.value]
+
+
+def kvtc_blob_max_bytes(n: int, D: int) -> int:
+    return _check(lib().kvtc_blob_max_bytes(n, D), "kvtc_blob_max_bytes")
 
 
 def kvtc_calib_free(calib: Calib) -> None:

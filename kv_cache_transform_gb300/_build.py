@@ -14,7 +14,8 @@ BUILD = os.path.join(ROOT, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
          "-I" + os.path.join(ROOT, "include")]
-SOURCES = ["kvtc_host.cu", "kvtc_kernels.cu"]
+SOURCES = ["kvtc_host.cu", "kvtc_kernels.cu", "kvtc_calib.cu"]
+LIBS = ["-lcublas", "-lcusolver"]
 DEPS = SOURCES + ["kvtc_internal.cuh", "ptx.cuh"]
 
 
@@ -56,7 +57,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with cf.ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = OUT + ".tmp"
-    cmd = [nvcc, "-shared", *ARCH, "-o", tmp, *objs]
+    cmd = [nvcc, "-shared", *ARCH, "-o", tmp, *objs, *LIBS]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")

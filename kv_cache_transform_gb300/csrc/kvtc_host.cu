@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -17,9 +18,10 @@
 
 using namespace kvtc;
 
-namespace {
+namespace kvtc {
+static std::atomic<uint64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
-// ------------------------------------------------------------ utilities
 uint32_t crc32_ieee(const uint8_t* p, size_t n) {
   // CRC-32 of IEEE 802.3 (reflected polynomial 0xEDB88320, init and final
   // xor 0xFFFFFFFF), table driven.
@@ -36,6 +38,9 @@ uint32_t crc32_ieee(const uint8_t* p, size_t n) {
   for (size_t i = 0; i < n; ++i) c = table[(c ^ p[i]) & 0xFFu] ^ (c >> 8);
   return c ^ 0xFFFFFFFFu;
 }
+}  // namespace kvtc
+
+namespace {
 
 // Nearest (ties to even) bf16 of a finite double, rounded once: keep 8
 // significant bits (quantum 2^-133 below the normal range).
@@ -214,6 +219,10 @@ int grid_for(const kvtc_calib* c, int tiles) {
 }  // namespace
 
 extern "C" {
+
+uint64_t kvtc_launch_count(void) {
+  return kvtc::g_launches.load(std::memory_order_relaxed);
+}
 
 const char* kvtc_strerror(int s) {
   switch (s) {

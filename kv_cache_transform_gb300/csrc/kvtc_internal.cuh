@@ -118,6 +118,10 @@ cudaError_t launch_decompress_paged(const PagedParams& p, int grid,
                                     cudaStream_t st);
 cudaError_t launch_raw_copy(const RawParams& p, cudaStream_t st);
 cudaError_t launch_paged_raw(const PagedParams& p, cudaStream_t st);
+// Kernel launches issued by this library (all devices, all threads).
+void count_launch();
+// CRC-32 of IEEE 802.3 (as zlib): reflected 0xEDB88320, init/final ~0.
+uint32_t crc32_ieee(const uint8_t* p, size_t n);
 int compress_smem_bytes(int nstages, int stage_bytes, int rec_stg_words);
 int decompress_smem_bytes();
 

@@ -785,6 +785,7 @@ cudaError_t launch_compress(const CompParams& p, int grid, cudaStream_t st) {
     configured = 232448;
   }
   compress_kernel<<<grid, kCompThreads, smem, st>>>(p);
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -799,6 +800,7 @@ static cudaError_t launch_dec(const P& p, int grid, cudaStream_t st) {
     configured = true;
   }
   decompress_kernel<P><<<grid, kDecThreads, kDecSmem, st>>>(p);
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -816,6 +818,7 @@ cudaError_t launch_raw_copy(const RawParams& p, cudaStream_t st) {
   int64_t blocks = (p.total_chunks + 255) / 256;
   if (blocks > 4096) blocks = 4096;
   raw_copy_kernel<<<(int)blocks, 256, 0, st>>>(p);
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -824,6 +827,7 @@ cudaError_t launch_paged_raw(const PagedParams& p, cudaStream_t st) {
   int64_t blocks = (p.total_raw_chunks + 255) / 256;
   if (blocks > 4096) blocks = 4096;
   paged_raw_kernel<<<(int)blocks, 256, 0, st>>>(p);
+  count_launch();
   return cudaGetLastError();
 }
 

@@ -182,12 +182,25 @@ def eval_tokens_torch(w: Workload, layer: int, kv: int, request: int = 0,
     multi-GB workloads).  The numbers differ from :func:`eval_tokens` (another
     generator) but the distribution and seed are the same.  Returns a bf16
     tensor [T][D]."""
-    import torch
     p = params if params is not None else stream_params(w, layer, kv)
     n = w.tokens if T is None else T
+    return _draw_torch(p, eval_seed(layer, kv, request), n, device)
+
+
+def calib_tokens_torch(w: Workload, layer: int, kv: int, device="cuda",
+                       params: Optional[StreamParams] = None):
+    """Calibration tokens drawn with torch's generator on ``device`` (same
+    recipe and seed as :func:`calib_tokens`, other generator); bf16
+    [n_calib][D]."""
+    return _draw_torch(stream_params(w, layer, kv) if params is None
+                       else params, calib_seed(layer, kv), w.n_calib, device)
+
+
+def _draw_torch(p: StreamParams, seed: int, n: int, device):
+    import torch
     D, r = p.A.shape
     g = torch.Generator(device=device)
-    g.manual_seed(eval_seed(layer, kv, request))
+    g.manual_seed(seed)
     z = torch.randn((n, r), generator=g, device=device, dtype=torch.float32)
     eps = torch.randn((n, D), generator=g, device=device, dtype=torch.float32)
     A = torch.from_numpy(p.A.astype(np.float32)).to(device)
