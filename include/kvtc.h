@@ -200,6 +200,30 @@ int64_t kvtc_blob_max_bytes(int n, int D);
 int kvtc_device_status(const kvtc_calib* calib, void* cuda_stream,
                        unsigned* flags);
 
+/*
+ * kvtc_calib_mean_static -- the per-channel mean of calibration rows (the
+ * mean that kvtc_calibrate stores for a stream), computed without
+ * allocating any device memory.  The paper has no counterpart: this entry
+ * point exists for callers that cannot call cudaMalloc, such as serving
+ * engines that give nearly all device memory to their own KV-cache pool at
+ * start-up, or latency-sensitive paths that cannot take the device-wide
+ * synchronisation of cudaMalloc / cudaFree.
+ *   tokens : device bf16 rows [N][ld] (N >= 1, ld >= D).
+ *   mu_out : device fp64 [D], written.
+ *   D      : at most 4096; wider rows return KVTC_ESIZE.
+ * Scratch comes from a fixed 1 MiB array inside the library, held by every
+ * GPU that loads the library until the process exits.  The first call on a
+ * device looks up that array's device address (a one-time set-up); make
+ * that first call before any stream capture.  All calls share the array:
+ * each call writes every entry it reads, but calls that overlap on the GPU
+ * race with each other.  No cudaMalloc, cudaFree or allocating library
+ * routine is called.  Enqueued on cuda_stream.
+ * Errors: EINVAL, ESIZE, ECUDA.
+ */
+int kvtc_calib_mean_static(int cuda_device, const void* tokens, int64_t N,
+                           int64_t ld, int D, double* mu_out,
+                           void* cuda_stream);
+
 /* Number of kernels this library has launched since it was loaded (all
  * devices and threads); a cheap way for callers to count launches. */
 uint64_t kvtc_launch_count(void);

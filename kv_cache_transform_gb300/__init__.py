@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
                                  ctypes.POINTER(ctypes.c_size_t), c_vp]),
         "kvtc_blob_max_bytes": (c_i64, [c_i, c_i]),
         "kvtc_launch_count": (ctypes.c_uint64, []),
+        "kvtc_calib_mean_static": (c_i, [c_i, c_vp, c_i64, c_i64, c_i, c_vp,
+                                         c_vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -186,6 +188,16 @@ def kvtc_calibrate(tokens: Sequence, layers: Sequence[int],
 
 def kvtc_blob_max_bytes(n: int, D: int) -> int:
     return _check(lib().kvtc_blob_max_bytes(n, D), "kvtc_blob_max_bytes")
+
+
+def kvtc_calib_mean_static(tokens, N: int, ld: int, D: int, mu_out,
+                           device: int = 0, stream=None) -> None:
+    """Per-channel mean of device bf16 rows [N][ld] into device fp64 mu_out,
+    with no device allocation (for callers that own all device memory)."""
+    _check(lib().kvtc_calib_mean_static(device, _ptr(tokens) or None, N, ld,
+                                         D, _ptr(mu_out) or None,
+                                         _stream(stream) or None),
+           "kvtc_calib_mean_static")
 
 
 def kvtc_calib_free(calib: Calib) -> None:
