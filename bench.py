@@ -204,6 +204,9 @@ def run_ours(args):
         dist.barrier()
     kv.lib()
     w = synth.WORKLOADS[args.workload]
+    if args.layers:
+        import dataclasses
+        w = dataclasses.replace(w, layers=min(args.layers, w.layers))
     streams = w.streams()
     T, D = w.tokens, w.D
     stream = torch.cuda.current_stream()
@@ -413,6 +416,9 @@ def main():
                     choices=sorted(k for k, v in synth.WORKLOADS.items()
                                    if v.requests == 1))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="restrict to the first L layers (small profiling "
+                         "cases; the default is the whole workload)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -1,5 +1,6 @@
 // Host side of the C ABI declared in include/kvtc.h: calibration blob
 // parsing, device operand preparation, argument validation and launches.
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -135,6 +136,22 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// Output map for the reconstruction epilogue: bf16 rows [rows][cols] with a
+// stride of row_bytes, box {64 columns, 32 rows}, 128-byte swizzle.
+bool encode_store_2d(CUtensorMap* m, const void* base, uint64_t cols,
+                     uint64_t rows, uint64_t row_bytes) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {64u, 32u};
+  cuuint32_t estr[2] = {1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 struct DeviceGuard {
@@ -298,6 +315,12 @@ int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
       break;
     }
     h.widths.assign(w, w + G);
+    for (int d = 0; d < h.D; ++d) {
+      double m;
+      std::memcpy(&m, mu + 8LL * d, 8);
+      if (!std::isfinite(m) || std::fabs(m) > 60000.0) status = KVTC_ENOTSUP;
+    }
+    if (status != KVTC_OK) break;
     int ga = 0, cost = 0;
     for (int g = 0; g < G; ++g) {
       if (h.widths[g] > bmax) status = KVTC_EFORMAT;
@@ -353,7 +376,7 @@ int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
     o.bits = total; total = align_up(total + h.Ga, 256);
     o.poff = total; total = align_up(total + 2LL * h.Ga, 256);
     o.venc = total; total = align_up(total + 2LL * h.k * h.D, 256);
-    o.vdec = total; total = align_up(total + 2LL * h.k * h.D, 256);
+    o.vdec = total; total = align_up(total + 2LL * (h.k + 16) * h.D, 256);
   }
   std::vector<uint8_t> host((size_t)total, 0);
   if (cudaMalloc(&c->pool, (size_t)total) != cudaSuccess) {
@@ -374,9 +397,17 @@ int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
     uint16_t* venc = reinterpret_cast<uint16_t*>(host.data() + o.venc);
     uint16_t* vdec = reinterpret_cast<uint16_t*>(host.data() + o.vdec);
     std::vector<double> muv(h.D);
+    const int kp = h.k + 16;
     for (int d = 0; d < h.D; ++d) {
       std::memcpy(&muv[d], mu + d, 8);
       hmu[d] = (float)muv[d];
+      // the reconstruction adds mu through one more K step: columns k and
+      // k + 1 of V_dec hold mu split into two fp16 terms (the A operand
+      // holds 1.0 there), the other 14 columns of that step are zero
+      const uint16_t hi = fp16_bits_rne(muv[d]);
+      const double hiv = (double)__half2float(__ushort_as_half(hi));
+      vdec[(size_t)d * kp + h.k] = hi;
+      vdec[(size_t)d * kp + h.k + 1] = fp16_bits_rne(muv[d] - hiv);
     }
     for (int a = 0; a < h.k; ++a) {
       double acc = 0.0;
@@ -385,7 +416,7 @@ int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
         std::memcpy(&v, V + (size_t)a * h.D + d, 8);
         const uint16_t eb = bf16_bits_rne(v);
         venc[(size_t)a * h.D + d] = eb;
-        vdec[(size_t)d * h.k + a] = fp16_bits_rne(v);
+        vdec[(size_t)d * kp + a] = fp16_bits_rne(v);
         uint32_t u = (uint32_t)eb << 16;
         float ef;
         std::memcpy(&ef, &u, 4);
@@ -415,8 +446,9 @@ int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
     s.Ga = h.Ga;
     s.R = h.R;
     s.nc = (h.D % 128 == 0) ? 128 : 64;
+    s.kp = kp;
     if (!encode_2d(&s.tm_vdec, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, dev + o.vdec,
-                   (uint64_t)h.k, (uint64_t)h.D, 2ull * h.k, (uint32_t)s.nc) ||
+                   (uint64_t)kp, (uint64_t)h.D, 2ull * kp, (uint32_t)s.nc) ||
         !encode_2d(&s.tm_venc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dev + o.venc,
                    (uint64_t)h.D, (uint64_t)h.k, 2ull * h.D, (uint32_t)h.k)) {
       cudaFree(c->pool);
@@ -567,7 +599,6 @@ int kvtc_compress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
       g.tc = (int32_t)tc;
       g.row0 = (int32_t)s_;
       g.cs = cs[i];
-      g.tile_begin = tiles;
       tiles += (int)((tc + kTileM - 1) / kTileM);
       kmax = std::max(kmax, h.k);
       rmax = std::max(rmax, h.R);
@@ -577,6 +608,7 @@ int kvtc_compress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
     p->status = c->d_status;
     p->nseg = (int32_t)(i1 - i0);
     p->total_tiles = tiles;
+    p->tiles_per_seg = (int32_t)((tc + kTileM - 1) / kTileM);
     p->b_bytes_max = kmax * 128;
     p->stage_bytes = kTileM * 128 + p->b_bytes_max;
     p->rec_stg_words = rmax / 4;
@@ -691,13 +723,19 @@ int kvtc_decompress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
         g.ld_bytes = 2 * ld;
         g.tc = (int32_t)tc;
         g.cs = cs[i];
-        g.tile_begin = tiles;
+        if (!encode_store_2d(&p->tm_out[i - i0], g.dst, (uint64_t)h.D,
+                             (uint64_t)tc, 2ull * ld)) {
+          ret = KVTC_ECUDA;
+          break;
+        }
         tiles += (int)((tc + kTileM - 1) / kTileM);
       }
+      if (ret != KVTC_OK) break;
       p->streams = c->d_streams;
       p->status = c->d_status;
       p->nseg = (int32_t)(i1 - i0);
       p->total_tiles = tiles;
+      p->tiles_per_seg = (int32_t)((tc + kTileM - 1) / kTileM);
       if (tiles && launch_decompress(*p, grid_for(c, tiles), stream) !=
                        cudaSuccess)
         ret = KVTC_ECUDA;

@@ -9,14 +9,15 @@ namespace kvtc {
 constexpr int kGroup = 16;         // components per microscaling group
 constexpr int kTileM = 128;        // tokens per tile (MMA M, TMEM lanes)
 constexpr int kAtomK = 64;         // 16-bit elements per 128-byte swizzle row
-constexpr int kMaxK = 256;         // kept components supported
+constexpr int kMaxK = 240;         // kept components supported
 constexpr int kMaxRecord = 256;    // record bytes supported by the kernels
 constexpr int kMaxD = 8192;
 
 // Device-resident description of one calibrated (layer, K|V) stream; built
 // once by kvtc_calib_load and read by every kernel launch.
 struct DevStream {
-  CUtensorMap tm_vdec;      // fp16 V_kept as [D rows][k cols], box {64, nc}
+  CUtensorMap tm_vdec;      // fp16 [D rows][kp cols]: V_kept, then mu_hi,
+                            // mu_lo and zeros (kp = k + 16), box {64, nc}
   CUtensorMap tm_venc;      // bf16 V_kept as [k rows][D cols], box {64, k}
   const float* mu;          // [D]   fp32 mean
   const float* m;           // [k]   fp32 projection of the mean
@@ -24,7 +25,8 @@ struct DevStream {
   const uint16_t* poff;     // [Ga]  byte offset of the group's first plane
   int32_t D, k, Ga, R;      // R = record bytes
   int32_t nc;               // reconstruction N chunk: 128 or 64
-  int32_t pad[3];
+  int32_t kp;               // reconstruction K: k + 16 (the mean step)
+  int32_t pad[2];
 };
 
 // ---------------------------------------------------------------- compress
@@ -35,7 +37,7 @@ struct CompSeg {
   int32_t tc;               // compressed tokens
   int32_t row0;             // s' (first compressed source row)
   int32_t cs;               // calibration stream index
-  int32_t tile_begin;       // first work item of this segment
+  int32_t pad;
 };
 struct CompParams {
   CompSeg seg[kCompMaxSeg];
@@ -43,6 +45,7 @@ struct CompParams {
   unsigned* status;
   int32_t nseg;
   int32_t total_tiles;
+  int32_t tiles_per_seg;    // every stream of a call has the same T
   int32_t nstages;
   int32_t stage_bytes;      // A + B bytes of one pipeline stage
   int32_t b_bytes_max;      // B bytes reserved per stage
@@ -50,22 +53,22 @@ struct CompParams {
 };
 
 // -------------------------------------------------------------- decompress
-constexpr int kDecMaxSeg = 256;
+constexpr int kDecMaxSeg = 96;
 struct DecSeg {
   const uint8_t* rec;       // first record
   char* dst;                // output row of the first compressed token
   int64_t ld_bytes;         // output row stride
   int32_t tc;
   int32_t cs;
-  int32_t tile_begin;
-  int32_t pad;
 };
 struct DecParams {
+  CUtensorMap tm_out[kDecMaxSeg];  // bf16 [T_c rows][D] from dst, box {64,32}
   DecSeg seg[kDecMaxSeg];
   const DevStream* streams;
   unsigned* status;
   int32_t nseg;
   int32_t total_tiles;
+  int32_t tiles_per_seg;    // every stream of a call has the same T
 };
 
 // Paged restore: work items are (request, stream, tile).

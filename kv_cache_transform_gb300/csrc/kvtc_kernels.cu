@@ -24,6 +24,30 @@
 
 namespace kvtc {
 
+// Optional per-role timing (compiled in only with -DKVTC_TRACE): each warp
+// accumulates the SM cycles it spends in up to eight phases and lane 0
+// stores the sums per CTA.  Timestamps only; no work is skipped.
+#ifdef KVTC_TRACE
+__device__ unsigned long long g_kvtc_trace[2][160][16][8];
+#define KVTC_TR_DECL                              \
+  unsigned long long tr_[8] = {0, 0, 0, 0, 0, 0, 0, 0}; \
+  unsigned long long tr_t = clock64();
+#define KVTC_TR(i)                                    \
+  {                                                   \
+    const unsigned long long tr_n = clock64();        \
+    tr_[i] += tr_n - tr_t;                            \
+    tr_t = tr_n;                                      \
+  }
+#define KVTC_TR_SAVE(k)                                  \
+  if (lane == 0 && blockIdx.x < 160)                     \
+    for (int i_ = 0; i_ < 8; ++i_)                       \
+      g_kvtc_trace[k][blockIdx.x][warp][i_] = tr_[i_];
+#else
+#define KVTC_TR_DECL
+#define KVTC_TR(i)
+#define KVTC_TR_SAVE(k)
+#endif
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   uintptr_t a = reinterpret_cast<uintptr_t>(p);
   uint32_t s = smem_u32(p);
@@ -85,6 +109,17 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t w, uint32_t sel,
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Tensor store shared -> global of one box, tracked by the thread's bulk
+// group.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t x,
+                                             int32_t y, const void* ssrc) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], "
+      "[%3];" ::"l"(tmap),
+      "r"(x), "r"(y), "r"(smem_u32(ssrc))
+      : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -93,17 +128,17 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 // ======================================================================
 //                               decompress
 // ======================================================================
-constexpr int kDecWarps = 10;  // 0 TMA, 1 MMA, 2-5 prologue, 6-9 epilogue
+constexpr int kDecWarps = 14;  // 0 TMA, 1 MMA, 2-5 prologue, 6-13 epilogue
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kDecNC = 128;
 constexpr int kDecStages = 4;
 constexpr int kDecBStage = kDecNC * 128;           // [128 rows][64 fp16]
-constexpr int kDecStgRow = kDecNC * 2 + 16;        // padded staging row
-constexpr int kDecStgWarp = 32 * kDecStgRow;
+constexpr int kDecStgHalf = 32 * 128;             // 32 rows x 64 bf16, SW128
+constexpr int kDecStgWarp = 2 * kDecStgHalf;       // one 128-column chunk
 constexpr int kRecWords = kMaxRecord / 4;
 constexpr int kRecStgWarp = kRecWords * 33 * 4;    // [words][33] u32
 constexpr int kDecOffStg = kDecStages * kDecBStage;
-constexpr int kDecOffRec = kDecOffStg + 4 * 2 * kDecStgWarp;
+constexpr int kDecOffRec = kDecOffStg + 8 * kDecStgWarp;
 constexpr int kDecOffBar = kDecOffRec + 4 * kRecStgWarp;
 constexpr int kDecOffMisc = kDecOffBar + 256;
 constexpr int kDecSmem = kDecOffMisc + 64 + 1024;
@@ -118,14 +153,11 @@ struct DecTile {
   int64_t ld_bytes;
   char* cache;         // paged: pool of this stream
   int tc, tile, cs, s_, req;
+  int seg;             // contiguous: segment (output tensor map) index
 };
 
 __device__ __forceinline__ DecTile resolve(const DecParams& p, int item) {
-  int lo = 0, hi = p.nseg - 1;
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (p.seg[mid].tile_begin <= item) lo = mid; else hi = mid - 1;
-  }
+  const int lo = item / p.tiles_per_seg;
   const DecSeg& g = p.seg[lo];
   DecTile t;
   t.rec = g.rec;
@@ -133,8 +165,9 @@ __device__ __forceinline__ DecTile resolve(const DecParams& p, int item) {
   t.ld_bytes = g.ld_bytes;
   t.cache = nullptr;
   t.tc = g.tc;
-  t.tile = item - g.tile_begin;
+  t.tile = item - lo * p.tiles_per_seg;
   t.cs = g.cs;
+  t.seg = lo;
   t.s_ = 0;
   t.req = 0;
   return t;
@@ -161,6 +194,7 @@ __device__ __forceinline__ DecTile resolve(const PagedParams& p, int item) {
   t.cache = p.cache[j];
   t.s_ = p.s_[r];
   t.req = p.req_index[r];
+  t.seg = -1;
   return t;
 }
 
@@ -237,30 +271,36 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------- TMA producer
     if (lane == 0) {
+      KVTC_TR_DECL
       uint32_t it_b = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
         const DecTile t = resolve(p, item);
         const DevStream* ds = p.streams + t.cs;
         const int nc = ds->nc, nch = ds->D / nc;
-        const int nkb = (ds->k + kAtomK - 1) / kAtomK;
+        const int nkb = (ds->kp + kAtomK - 1) / kAtomK;
         const uint32_t bytes = (uint32_t)nc * 128u;
         if (item == (int)blockIdx.x) prefetch_tmap(&ds->tm_vdec);
         for (int ch = 0; ch < nch && ok; ++ch) {
           for (int kb = 0; kb < nkb; ++kb) {
-            const uint32_t s = it_b % kDecStages;
+            const uint32_t s = it_b & (kDecStages - 1);
             const uint32_t ph = (it_b / kDecStages) & 1u;
+            KVTC_TR(0)
             if (!mbar_wait(&empty_b[s], ph ^ 1u, abort_flag)) {
               ok = false;
               break;
             }
             mbar_arrive_expect_tx(&full_b[s], bytes);
+            KVTC_TR(1)
             tma_load_2d(sB + s * kDecBStage, &ds->tm_vdec, kb * kAtomK,
                         ch * nc, &full_b[s]);
             ++it_b;
+            KVTC_TR(2)
           }
         }
       }
+      KVTC_TR(0)
+      KVTC_TR_SAVE(0)
       if (!ok) raise_abort(abort_flag, p.status);
       for (uint32_t s = 0; s < kDecStages; ++s) {
         if (it_b > s) {
@@ -272,49 +312,59 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------- MMA issuer
     if (lane == 0) {
+      KVTC_TR_DECL
       uint32_t it_b = 0, chunk = 0, it = 0;
       bool ok = true;
+      const uint64_t desc_b0 = sw128_desc(smem_u32(sB));
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
         const DecTile t = resolve(p, item);
         const DevStream* ds = p.streams + t.cs;
         const int nc = ds->nc, nch = ds->D / nc;
-        const int nkb = (ds->k + kAtomK - 1) / kAtomK;
-        const int ksteps = ds->k / kGroup;
+        const int nkb = (ds->kp + kAtomK - 1) / kAtomK;
+        const int ksteps = ds->kp / kGroup;  // kept groups + the mean step
         const uint32_t idesc = make_idesc(128, (uint32_t)nc, 0);
         const uint32_t abuf = it & 1u;
+        KVTC_TR(0)
         if (!mbar_wait(&a_full[abuf], (it >> 1) & 1u, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        KVTC_TR(1)
         const uint32_t a_col = tmem + 256u + abuf * 128u;
         for (int ch = 0; ch < nch && ok; ++ch) {
           const uint32_t accb = chunk & 1u;
+          KVTC_TR(0)
           if (!mbar_wait(&acc_empty[accb], ((chunk >> 1) & 1u) ^ 1u,
                          abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          KVTC_TR(2)
           const uint32_t d = tmem + accb * 128u;
+          uint32_t acol = a_col;
           for (int kb = 0; kb < nkb; ++kb) {
-            const uint32_t s = it_b % kDecStages;
+            const uint32_t s = it_b & (kDecStages - 1);
+            KVTC_TR(0)
             if (!mbar_wait(&full_b[s], (it_b / kDecStages) & 1u,
                            abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t base = smem_u32(sB + s * kDecBStage);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              const int step = kb * 4 + ks;
-              if (step < ksteps)
-                mma_ts(d, a_col + (uint32_t)step * 8u,
-                       sw128_desc(base + ks * 32), idesc, step > 0);
-            }
+            KVTC_TR(3)
+            // descriptor start address advances 32 bytes (2 units) per K=16
+            const uint64_t bdesc = desc_b0 + (uint64_t)(s * (kDecBStage >> 4));
+            const int nks = min(4, ksteps - kb * 4);
+            mma_ts(d, acol, bdesc, idesc, kb > 0);
+            if (nks > 1) mma_ts(d, acol + 8u, bdesc + 2u, idesc, 1u);
+            if (nks > 2) mma_ts(d, acol + 16u, bdesc + 4u, idesc, 1u);
+            if (nks > 3) mma_ts(d, acol + 24u, bdesc + 6u, idesc, 1u);
+            acol += 32u;
             tc_commit(&empty_b[s]);
             ++it_b;
+            KVTC_TR(4)
           }
           if (!ok) break;
           tc_commit(&acc_full[accb]);
@@ -324,6 +374,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         tc_commit(&a_empty[abuf]);
         ++it;
       }
+      KVTC_TR(0)
+      KVTC_TR_SAVE(0)
       if (!ok) raise_abort(abort_flag, p.status);
       tc_commit(mma_done);
       mbar_drain(mma_done, 0);
@@ -335,32 +387,48 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     uint32_t* stg = sRec + (warp - 2) * (kRecWords * 33);
     uint32_t it = 0;
     bool ok = true;
+    KVTC_TR_DECL
     for (int item = blockIdx.x; item < total; item += gridDim.x) {
       const DecTile t = resolve(p, item);
       const DevStream* ds = p.streams + t.cs;
       const int R = ds->R, Ga = ds->Ga;
       const uint32_t abuf = it & 1u;
+      KVTC_TR(0)
       if (!mbar_wait(&a_empty[abuf], ((it >> 1) & 1u) ^ 1u, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      KVTC_TR(1)
       const int row0 = t.tile * kTileM + q * 32;
       const int nvalid = min(max(t.tc - row0, 0), 32);
       const uint8_t* rbase = t.rec + (int64_t)row0 * R;
-      // Coalesced 16-byte loads of the warp's 32 records, stored
-      // word-transposed ([word][token], row pitch 33) in shared memory.
-      for (int o = lane * 16; o < 32 * R; o += 512) {
-        const int tr = o / R;
-        const int wd = (o - tr * R) >> 2;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (tr < nvalid) v = ld_nc_v4(rbase + o);
-        stg[(wd + 0) * 33 + tr] = v.x;
-        stg[(wd + 1) * 33 + tr] = v.y;
-        stg[(wd + 2) * 33 + tr] = v.z;
-        stg[(wd + 3) * 33 + tr] = v.w;
+      // Coalesced 16-byte loads of the warp's 32 records (up to eight in
+      // flight per lane), stored word-transposed ([word][token], row pitch
+      // 33) in shared memory.
+      const int nld = (32 * R) >> 9;  // 16-byte loads per lane
+      for (int b0 = 0; b0 < nld; b0 += 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int o = (b0 + u) * 512 + lane * 16;
+          v[u] = make_uint4(0u, 0u, 0u, 0u);
+          if (b0 + u < nld && o / R < nvalid) v[u] = ld_nc_v4(rbase + o);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (b0 + u >= nld) break;
+          const int o = (b0 + u) * 512 + lane * 16;
+          const int tr = o / R;
+          const int wd = (o - tr * R) >> 2;
+          stg[(wd + 0) * 33 + tr] = v[u].x;
+          stg[(wd + 1) * 33 + tr] = v[u].y;
+          stg[(wd + 2) * 33 + tr] = v[u].z;
+          stg[(wd + 3) * 33 + tr] = v[u].w;
+        }
       }
       __syncwarp();
+      KVTC_TR(2)
       const uint32_t a_tmem =
           tmem + ((uint32_t)(q * 32) << 16) + 256u + abuf * 128u;
       for (int a = 0; a < Ga; ++a) {
@@ -392,69 +460,119 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         out[7] = dequant_pair(w3, 0x4342u, sc2, sh2);
         tmem_st8(a_tmem + (uint32_t)a * 8u, out);
       }
+      {
+        // the mean step: A = (1, 1, 0, ..., 0) against (mu_hi, mu_lo, 0...)
+        const uint32_t ones[8] = {0x3C003C00u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        tmem_st8(a_tmem + (uint32_t)Ga * 8u, ones);
+      }
+      KVTC_TR(3)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&a_full[abuf]);
       ++it;
+      KVTC_TR(4)
     }
+    KVTC_TR(0)
+    KVTC_TR_SAVE(0)
     if (!ok && lane == 0) raise_abort(abort_flag, p.status);
   } else {
-    // ------------------------------- epilogue: + mu, bf16, bulk stores
+    // -------------- epilogue: bf16 rows (the mean came in the MMA)
+    // Two sets of four warps (one per TMEM lane quadrant each): set 0
+    // drains the even chunks (accumulator 0), set 1 the odd ones.  A warp
+    // stages its 32 rows x 128 columns as two 128-byte-swizzled boxes and
+    // writes them with TMA tensor stores (contiguous output) or with
+    // coalesced 16-byte stores through the block table (paged output).
+    constexpr bool kPaged = std::is_same<P, PagedParams>::value;
     const int q = warp & 3;
-    uint8_t* stg_base = sStg + (warp - 6) * 2 * kDecStgWarp;
+    const uint32_t set = (uint32_t)(warp - 6) >> 2;
+    uint8_t* stg_w = sStg + (warp - 6) * kDecStgWarp;
+    const uint32_t stg_row = smem_u32(stg_w) + lane * 128;
+    const uint32_t sw = (uint32_t)(lane & 7);
     uint32_t chunk = 0;
     bool ok = true;
+    KVTC_TR_DECL
     for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
       const DecTile t = resolve(p, item);
       const DevStream* ds = p.streams + t.cs;
       const int D = ds->D, nc = ds->nc, nch = D / nc;
       const int row = t.tile * kTileM + q * 32 + lane;
-      const bool valid = row < t.tc;
-      char* rowp = valid ? dec_row_ptr(p, t, row, D) : nullptr;
-      const float* mu = ds->mu;
-      for (int ch = 0; ch < nch; ++ch) {
+      char* rowp = nullptr;
+      if constexpr (kPaged) {
+        if (row < t.tc) rowp = dec_row_ptr(p, t, row, D);
+      }
+      for (int ch = 0; ch < nch; ++ch, ++chunk) {
         const uint32_t accb = chunk & 1u;
+        if (accb != set) continue;
+        KVTC_TR(0)
         if (!mbar_wait(&acc_full[accb], (chunk >> 1) & 1u, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint8_t* stg = stg_base + (chunk & 1u) * kDecStgWarp + lane * kDecStgRow;
-        const uint32_t stg_addr = smem_u32(stg);
-        bulk_wait_read<1>();
+        if constexpr (!kPaged) {
+          if (lane == 0) bulk_wait_read<0>();  // staging free again
+        }
+        __syncwarp();
+        KVTC_TR(1)
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + accb * 128u;
         const int npc = nc / 32;
-        for (int pc = 0; pc < npc; ++pc) {
-          float v[32];
+        for (int pc = 0; pc < npc; pc += 2) {
+          float v[64];
           tmem_ld32(taddr + (uint32_t)pc * 32u, v);
+          tmem_ld32(taddr + (uint32_t)(pc + 1) * 32u, v + 32);
           tmem_wait_ld();
-          if (pc == npc - 1) {
+          if (pc + 2 >= npc) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[accb]);
           }
-          const float4* m4 =
-              reinterpret_cast<const float4*>(mu + ch * nc + pc * 32);
-          uint32_t o[16];
+          const uint32_t half = stg_row + (uint32_t)(pc >> 1) * kDecStgHalf;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 mm = __ldg(m4 + i);
-            o[2 * i] = pack_bf16(v[4 * i] + mm.x, v[4 * i + 1] + mm.y);
-            o[2 * i + 1] = pack_bf16(v[4 * i + 2] + mm.z, v[4 * i + 3] + mm.w);
-          }
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            sts_v4(stg_addr + pc * 64 + i * 16, o[4 * i], o[4 * i + 1],
-                   o[4 * i + 2], o[4 * i + 3]);
+          for (int i = 0; i < 8; ++i)
+            sts_v4(half + ((i ^ sw) << 4), pack_bf16(v[8 * i], v[8 * i + 1]),
+                   pack_bf16(v[8 * i + 2], v[8 * i + 3]),
+                   pack_bf16(v[8 * i + 4], v[8 * i + 5]),
+                   pack_bf16(v[8 * i + 6], v[8 * i + 7]));
         }
-        fence_proxy_async_smem();
-        if (rowp) bulk_s2g(rowp + (int64_t)ch * nc * 2, stg, (uint32_t)nc * 2u);
-        bulk_commit();
-        ++chunk;
+        KVTC_TR(2)
+        if constexpr (!kPaged) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            for (int h = 0; h < nc / 64; ++h)
+              tma_store_2d(&p.tm_out[t.seg], ch * nc + h * 64,
+                           t.tile * kTileM + q * 32, stg_w + h * kDecStgHalf);
+            bulk_commit();
+          }
+        } else {
+          __syncwarp();
+          // a row chunk (nc * 2 bytes) is written by nc / 8 lanes, 16 bytes
+          // each, so every store instruction covers whole 128-byte lines
+          const int lanes_per_row = nc / 8;
+          const int rows_per_it = 32 / lanes_per_row;
+          const int sub = lane % lanes_per_row;
+          for (int r0 = 0; r0 < 32; r0 += rows_per_it) {
+            const int r = r0 + lane / lanes_per_row;
+            char* rp = reinterpret_cast<char*>(__shfl_sync(
+                0xFFFFFFFFu, reinterpret_cast<uintptr_t>(rowp), r));
+            const int c16 = sub & 7;
+            const uint4 val = *reinterpret_cast<const uint4*>(
+                stg_w + (sub >> 3) * kDecStgHalf + r * 128 +
+                ((c16 ^ (r & 7)) << 4));
+            if (rp)
+              *reinterpret_cast<uint4*>(rp + (int64_t)ch * nc * 2 + sub * 16) =
+                  val;
+          }
+        }
+        KVTC_TR(3)
       }
     }
-    bulk_wait<0>();
+    if constexpr (!kPaged) {
+      if (lane == 0) bulk_wait<0>();
+    }
+    KVTC_TR(0)
+    KVTC_TR_SAVE(0)
     if (!ok && lane == 0) raise_abort(abort_flag, p.status);
   }
 
@@ -469,23 +587,18 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 // ======================================================================
 //                                compress
 // ======================================================================
-constexpr int kCompWarps = 6;  // 0 TMA, 1 MMA, 2-5 epilogue
+constexpr int kCompWarps = 10;  // 0 TMA, 1 MMA, 2-9 epilogue (two sets)
 constexpr int kCompThreads = kCompWarps * 32;
 constexpr int kCompMaxStages = 6;
 constexpr int kCompAStage = kTileM * 128;          // [128 rows][64 bf16]
 constexpr uint32_t kCompTmemCols = 512;            // accumulators at 0, 256
 
 int compress_smem_bytes(int nstages, int stage_bytes, int rec_stg_words) {
-  return nstages * stage_bytes + 4 * rec_stg_words * 33 * 4 + 256 + 64 + 1024;
+  return nstages * stage_bytes + 8 * rec_stg_words * 33 * 4 + 256 + 64 + 1024;
 }
 
 __device__ __forceinline__ int find_comp_seg(const CompParams& p, int item) {
-  int lo = 0, hi = p.nseg - 1;
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (p.seg[mid].tile_begin <= item) lo = mid; else hi = mid - 1;
-  }
-  return lo;
+  return item / p.tiles_per_seg;
 }
 
 __global__ void __launch_bounds__(kCompThreads, 1)
@@ -497,7 +610,7 @@ __global__ void __launch_bounds__(kCompThreads, 1)
   uint32_t* sRec = reinterpret_cast<uint32_t*>(smem + nst * stage_bytes);
   const int rec_words = p.rec_stg_words;
   uint64_t* bar =
-      reinterpret_cast<uint64_t*>(smem + nst * stage_bytes + 4 * rec_words * 33 * 4);
+      reinterpret_cast<uint64_t*>(smem + nst * stage_bytes + 8 * rec_words * 33 * 4);
   uint64_t* full = bar;
   uint64_t* empty = bar + kCompMaxStages;
   uint64_t* acc_full = bar + 2 * kCompMaxStages;
@@ -535,28 +648,38 @@ __global__ void __launch_bounds__(kCompThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------- TMA producer
     if (lane == 0) {
-      uint32_t it_b = 0;
+      KVTC_TR_DECL
+      uint32_t it_b = 0, s = 0, ph = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-        const CompSeg& g = p.seg[find_comp_seg(p, item)];
-        const int tile = item - g.tile_begin;
+        const int sg = find_comp_seg(p, item);
+        const CompSeg& g = p.seg[sg];
+        const int tile = item - sg * p.tiles_per_seg;
         const DevStream* ds = p.streams + g.cs;
         const int nkb = ds->D / kAtomK;
         const uint32_t bytes = (uint32_t)kCompAStage + (uint32_t)ds->k * 128u;
         for (int kb = 0; kb < nkb; ++kb) {
-          const uint32_t s = it_b % nst;
-          if (!mbar_wait(&empty[s], ((it_b / nst) & 1u) ^ 1u, abort_flag)) {
+          KVTC_TR(0)
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
+          KVTC_TR(1)
           uint8_t* st = smem + s * stage_bytes;
           mbar_arrive_expect_tx(&full[s], bytes);
           tma_load_2d(st, &g.tm_x, kb * kAtomK, g.row0 + tile * kTileM,
                       &full[s]);
           tma_load_2d(st + kCompAStage, &ds->tm_venc, kb * kAtomK, 0, &full[s]);
           ++it_b;
+          if (++s == (uint32_t)nst) {
+            s = 0;
+            ph ^= 1u;
+          }
+          KVTC_TR(2)
         }
       }
+      KVTC_TR(0)
+      KVTC_TR_SAVE(1)
       if (!ok) raise_abort(abort_flag, p.status);
       for (uint32_t s = 0; s < (uint32_t)nst; ++s) {
         if (it_b > s) {
@@ -568,40 +691,53 @@ __global__ void __launch_bounds__(kCompThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------- MMA issuer
     if (lane == 0) {
-      uint32_t it_b = 0, it = 0;
+      KVTC_TR_DECL
+      uint32_t it = 0, s = 0, ph = 0;
       bool ok = true;
+      const uint64_t desc_s0 = sw128_desc(smem_u32(smem));
+      const uint64_t stage_units = (uint64_t)(stage_bytes >> 4);
+      const uint64_t b_units = (uint64_t)(kCompAStage >> 4);
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
         const CompSeg& g = p.seg[find_comp_seg(p, item)];
         const DevStream* ds = p.streams + g.cs;
         const int nkb = ds->D / kAtomK;
         const uint32_t idesc = make_idesc(128, (uint32_t)ds->k, 1);
         const uint32_t accb = it & 1u;
+        KVTC_TR(0)
         if (!mbar_wait(&acc_empty[accb], ((it >> 1) & 1u) ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        KVTC_TR(1)
         const uint32_t d = tmem + accb * 256u;
         for (int kb = 0; kb < nkb; ++kb) {
-          const uint32_t s = it_b % nst;
-          if (!mbar_wait(&full[s], (it_b / nst) & 1u, abort_flag)) {
+          KVTC_TR(0)
+          if (!mbar_wait(&full[s], ph, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a = smem_u32(smem + s * stage_bytes);
-          const uint32_t b = a + kCompAStage;
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_ss(d, sw128_desc(a + ks * 32), sw128_desc(b + ks * 32), idesc,
-                   (kb | ks) != 0);
+          KVTC_TR(2)
+          const uint64_t ad = desc_s0 + s * stage_units;
+          const uint64_t bd = ad + b_units;
+          mma_ss(d, ad, bd, idesc, kb > 0);
+          mma_ss(d, ad + 2u, bd + 2u, idesc, 1u);
+          mma_ss(d, ad + 4u, bd + 4u, idesc, 1u);
+          mma_ss(d, ad + 6u, bd + 6u, idesc, 1u);
           tc_commit(&empty[s]);
-          ++it_b;
+          if (++s == (uint32_t)nst) {
+            s = 0;
+            ph ^= 1u;
+          }
+          KVTC_TR(3)
         }
         if (!ok) break;
         tc_commit(&acc_full[accb]);
         ++it;
       }
+      KVTC_TR(0)
+      KVTC_TR_SAVE(1)
       if (!ok) raise_abort(abort_flag, p.status);
       tc_commit(mma_done);
       mbar_drain(mma_done, 0);
@@ -609,84 +745,109 @@ __global__ void __launch_bounds__(kCompThreads, 1)
     __syncwarp();
   } else {
     // ------------------------- epilogue: quantise + bit-plane records
+    // Two sets of four warps (one per TMEM lane quadrant each): set 0 takes
+    // the even tiles (accumulator 0), set 1 the odd ones.
     const int q = warp & 3;
+    const uint32_t set = (uint32_t)(warp - 2) >> 2;
     uint32_t* stg = sRec + (warp - 2) * (rec_words * 33);
     const uint32_t stg_addr = smem_u32(stg);
     uint32_t it = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < total; item += gridDim.x) {
-      const CompSeg& g = p.seg[find_comp_seg(p, item)];
-      const int tile = item - g.tile_begin;
+    KVTC_TR_DECL
+    for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
+      const uint32_t accb = it & 1u;
+      if (accb != set) continue;
+      const int sg = find_comp_seg(p, item);
+      const CompSeg& g = p.seg[sg];
+      const int tile = item - sg * p.tiles_per_seg;
       const DevStream* ds = p.streams + g.cs;
       const int R = ds->R, Ga = ds->Ga;
-      const uint32_t accb = it & 1u;
+      KVTC_TR(0)
       if (!mbar_wait(&acc_full[accb], (it >> 1) & 1u, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      KVTC_TR(1)
       const int row0 = tile * kTileM + q * 32;
       const int nvalid = min(max(g.tc - row0, 0), 32);
       for (int w = 0; w < (R >> 2); ++w) stg[w * 33 + lane] = 0u;
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + accb * 256u;
       bool range_err = false;
-      for (int a = 0; a < Ga; ++a) {
-        float v[16];
-        tmem_ld16(taddr + (uint32_t)a * 16u, v);
+      for (int a0 = 0; a0 < Ga; a0 += 2) {
+        // two groups per TMEM round trip (the second may lie past k when Ga
+        // is odd; it is inside the allocation and left unused)
+        float v2[32];
+        tmem_ld32(taddr + (uint32_t)a0 * 16u, v2);
         tmem_wait_ld();
-        const float4* m4 = reinterpret_cast<const float4*>(ds->m + a * 16);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 mm = __ldg(m4 + i);
-          v[4 * i] -= mm.x;
-          v[4 * i + 1] -= mm.y;
-          v[4 * i + 2] -= mm.z;
-          v[4 * i + 3] -= mm.w;
+        if (a0 + 2 >= Ga) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[accb]);
         }
-        float lo = v[0], hi = v[0];
 #pragma unroll
-        for (int i = 1; i < 16; ++i) {
-          lo = fminf(lo, v[i]);
-          hi = fmaxf(hi, v[i]);
-        }
-        const int b = ds->bits[a];
-        const int po = ds->poff[a];
-        const float lev = (float)((1 << b) - 1);
-        const __half sh = __float2half_rd(lo);
-        const float shf = __half2float(sh);
-        const __half sc = __float2half_ru(__fdiv_ru(__fsub_ru(hi, shf), lev));
-        const float scf = __half2float(sc);
-        range_err |= __hisinf(sh) != 0 || __hisinf(sc) != 0 ||
-                     __hisnan(sh) || __hisnan(sc);
-        const float inv = scf > 0.f ? __frcp_rn(scf) : 0.f;
-        uint32_t code[16];
+        for (int h = 0; h < 2; ++h) {
+          const int a = a0 + h;
+          if (a >= Ga) break;
+          float* v = v2 + 16 * h;
+          const float4* m4 = reinterpret_cast<const float4*>(ds->m + a * 16);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float u = fmaf(v[i] - shf, inv, 0.5f);
-          u = fminf(fmaxf(u, 0.f), lev);
-          code[i] = __float_as_uint(__fadd_rd(u, 8388608.f)) & 0xFFu;
-        }
-        uint32_t w[4];
+          for (int i = 0; i < 4; ++i) {
+            const float4 mm = __ldg(m4 + i);
+            v[4 * i] -= mm.x;
+            v[4 * i + 1] -= mm.y;
+            v[4 * i + 2] -= mm.z;
+            v[4 * i + 3] -= mm.w;
+          }
+          float lo = v[0], hi = v[0];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          w[kk] = code[4 * kk] | (code[4 * kk + 1] << 8) |
-                  (code[4 * kk + 2] << 16) | (code[4 * kk + 3] << 24);
-        stg[a * 33 + lane] = (uint32_t)__half_as_ushort(sh) |
-                             ((uint32_t)__half_as_ushort(sc) << 16);
-        for (int j = 0; j < b; ++j) {
-          uint32_t plane = 0;
+          for (int i = 1; i < 16; ++i) {
+            lo = fminf(lo, v[i]);
+            hi = fmaxf(hi, v[i]);
+          }
+          const int b = ds->bits[a];
+          const int po = ds->poff[a];
+          const float lev = (float)((1 << b) - 1);
+          const __half sh = __float2half_rd(lo);
+          const float shf = __half2float(sh);
+          // upper bound of (hi - shift) / lev, then rounded up to fp16
+          const float pre = __fmul_ru(__fsub_ru(hi, shf), __frcp_ru(lev));
+          const __half sc = __float2half_ru(pre);
+          const float scf = __half2float(sc);
+          range_err |= __hisinf(sh) != 0 || __hisinf(sc) != 0 ||
+                       __hisnan(sh) || __hisnan(sc);
+          const float inv = scf > 0.f ? __frcp_rn(scf) : 0.f;
+          uint32_t cb[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float u = fmaf(v[i] - shf, inv, 0.5f);
+            u = fminf(fmaxf(u, 0.f), lev);
+            cb[i] = __float_as_uint(__fadd_rd(u, 8388608.f));  // low byte = q
+          }
+          uint32_t w[4];
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            plane |= gather4((w[kk] >> j) & 0x01010101u) << (4 * kk);
-          const int bo = po + 2 * j;
-          sts_u16(stg_addr + (uint32_t)(((bo >> 2) * 33 + lane) * 4 + (bo & 2)),
-                  plane);
+            w[kk] = __byte_perm(__byte_perm(cb[4 * kk], cb[4 * kk + 1], 0x0040u),
+                                __byte_perm(cb[4 * kk + 2], cb[4 * kk + 3],
+                                            0x0040u),
+                                0x5410u);
+          stg[a * 33 + lane] = (uint32_t)__half_as_ushort(sh) |
+                               ((uint32_t)__half_as_ushort(sc) << 16);
+          for (int j = 0; j < b; ++j) {
+            uint32_t plane = 0;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              plane |= gather4((w[kk] >> j) & 0x01010101u) << (4 * kk);
+            const int bo = po + 2 * j;
+            sts_u16(
+                stg_addr + (uint32_t)(((bo >> 2) * 33 + lane) * 4 + (bo & 2)),
+                plane);
+          }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[accb]);
       if (range_err && lane < nvalid) atomicOr(p.status, KVTC_FLAG_RANGE);
+      __syncwarp();
+      KVTC_TR(2)
       uint8_t* rbase = g.rec + (int64_t)row0 * R;
       for (int o = lane * 16; o < 32 * R; o += 512) {
         const int tr = o / R;
@@ -696,8 +857,10 @@ __global__ void __launch_bounds__(kCompThreads, 1)
                 stg[(wd + 2) * 33 + tr], stg[(wd + 3) * 33 + tr]);
       }
       __syncwarp();
-      ++it;
+      KVTC_TR(3)
     }
+    KVTC_TR(0)
+    KVTC_TR_SAVE(1)
     if (!ok && lane == 0) raise_abort(abort_flag, p.status);
   }
 
@@ -775,6 +938,18 @@ __global__ void __launch_bounds__(256) paged_raw_kernel(
 // ======================================================================
 //                                launchers
 // ======================================================================
+#ifdef KVTC_TRACE
+}  // namespace kvtc
+extern "C" int kvtc_trace_read(void* host, size_t bytes) {
+  if (bytes < sizeof(kvtc::g_kvtc_trace)) return KVTC_ESIZE;
+  return cudaMemcpyFromSymbol(host, kvtc::g_kvtc_trace,
+                              sizeof(kvtc::g_kvtc_trace)) == cudaSuccess
+             ? KVTC_OK
+             : KVTC_ECUDA;
+}
+namespace kvtc {
+#endif
+
 cudaError_t launch_compress(const CompParams& p, int grid, cudaStream_t st) {
   const int smem = compress_smem_bytes(p.nstages, p.stage_bytes, p.rec_stg_words);
   static int configured = 0;
