@@ -229,8 +229,9 @@ int select_streams(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
   return KVTC_OK;
 }
 
-int grid_for(const kvtc_calib* c, int tiles) {
-  return std::max(1, std::min(tiles, c->sm_count));
+// CTA pairs for `items` super-tiles, at most what can be resident at once.
+int pairs_for(int max_pairs, int items) {
+  return std::max(1, std::min(items, max_pairs));
 }
 
 }  // namespace
@@ -447,10 +448,13 @@ int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
     s.R = h.R;
     s.nc = (h.D % 128 == 0) ? 128 : 64;
     s.kp = kp;
+    // each CTA of a pair loads half of the N rows of the B operand
     if (!encode_2d(&s.tm_vdec, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, dev + o.vdec,
-                   (uint64_t)kp, (uint64_t)h.D, 2ull * kp, (uint32_t)s.nc) ||
+                   (uint64_t)kp, (uint64_t)h.D, 2ull * kp,
+                   (uint32_t)(s.nc / 2)) ||
         !encode_2d(&s.tm_venc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dev + o.venc,
-                   (uint64_t)h.D, (uint64_t)h.k, 2ull * h.D, (uint32_t)h.k)) {
+                   (uint64_t)h.D, (uint64_t)h.k, 2ull * h.D,
+                   (uint32_t)(h.k / 2))) {
       cudaFree(c->pool);
       delete c;
       return KVTC_ECUDA;
@@ -599,7 +603,7 @@ int kvtc_compress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
       g.tc = (int32_t)tc;
       g.row0 = (int32_t)s_;
       g.cs = cs[i];
-      tiles += (int)((tc + kTileM - 1) / kTileM);
+      tiles += (int)((tc + kPairM - 1) / kPairM);
       kmax = std::max(kmax, h.k);
       rmax = std::max(rmax, h.R);
     }
@@ -608,8 +612,8 @@ int kvtc_compress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
     p->status = c->d_status;
     p->nseg = (int32_t)(i1 - i0);
     p->total_tiles = tiles;
-    p->tiles_per_seg = (int32_t)((tc + kTileM - 1) / kTileM);
-    p->b_bytes_max = kmax * 128;
+    p->tiles_per_seg = (int32_t)((tc + kPairM - 1) / kPairM);
+    p->b_bytes_max = kmax * 64;  // half of V_enc's k rows per CTA
     p->stage_bytes = kTileM * 128 + p->b_bytes_max;
     p->rec_stg_words = rmax / 4;
     int nst = 6;
@@ -617,7 +621,10 @@ int kvtc_compress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
                                           p->rec_stg_words) > 232448)
       --nst;
     p->nstages = nst;
-    if (launch_compress(*p, grid_for(c, tiles), stream) != cudaSuccess)
+    const int mp = max_pairs_compress(
+        compress_smem_bytes(nst, p->stage_bytes, p->rec_stg_words));
+    if (mp < 1 || launch_compress(*p, pairs_for(mp, tiles), stream) !=
+                      cudaSuccess)
       ret = KVTC_ECUDA;
   }
   delete p;
@@ -728,16 +735,22 @@ int kvtc_decompress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
           ret = KVTC_ECUDA;
           break;
         }
-        tiles += (int)((tc + kTileM - 1) / kTileM);
+        tiles += (int)((tc + kPairM - 1) / kPairM);
       }
       if (ret != KVTC_OK) break;
       p->streams = c->d_streams;
       p->status = c->d_status;
       p->nseg = (int32_t)(i1 - i0);
       p->total_tiles = tiles;
-      p->tiles_per_seg = (int32_t)((tc + kTileM - 1) / kTileM);
-      if (tiles && launch_decompress(*p, grid_for(c, tiles), stream) !=
-                       cudaSuccess)
+      p->tiles_per_seg = (int32_t)((tc + kPairM - 1) / kPairM);
+      int rmax = 0;
+      for (size_t i = i0; i < i1; ++i) rmax = std::max(rmax, c->hs[cs[i]].R);
+      p->rec_words = rmax / 4;
+      p->nstages = decompress_stages(p->rec_words);
+      const int mp = max_pairs_decompress(
+          decompress_smem_bytes(p->nstages, p->rec_words));
+      if (tiles && (mp < 1 || launch_decompress(*p, pairs_for(mp, tiles),
+                                                stream) != cudaSuccess))
         ret = KVTC_ECUDA;
     }
     if (ret == KVTC_OK && layer_events &&
@@ -801,7 +814,7 @@ int kvtc_decompress_paged(const kvtc_calib* c, int layer0, int nlayers,
       p->tile_begin[i] = tiles;
       p->raw_begin[i] = raw_chunks;
       p->req_index[i] = r;
-      tiles += (int)cs.size() * (int)((tc + kTileM - 1) / kTileM);
+      tiles += (int)cs.size() * (int)((tc + kPairM - 1) / kPairM);
       raw_chunks += (int64_t)cs.size() * (s_ + w_) * cpr;
     }
     p->tile_begin[r1 - r0] = tiles;
@@ -821,9 +834,17 @@ int kvtc_decompress_paged(const kvtc_calib* c, int layer0, int nlayers,
     p->total_tiles = tiles;
     p->D = D;
     p->total_raw_chunks = raw_chunks;
+    int rmax = 0;
+    for (size_t j = 0; j < cs.size(); ++j) rmax = std::max(rmax, c->hs[cs[j]].R);
+    p->rec_words = rmax / 4;
+    p->nstages = decompress_stages(p->rec_words);
     if (launch_paged_raw(*p, stream) != cudaSuccess) ret = KVTC_ECUDA;
+    const int mp =
+        max_pairs_decompress(decompress_smem_bytes(p->nstages, p->rec_words));
     if (ret == KVTC_OK && tiles &&
-        launch_decompress_paged(*p, grid_for(c, tiles), stream) != cudaSuccess)
+        (mp < 1 ||
+         launch_decompress_paged(*p, pairs_for(mp, tiles), stream) !=
+             cudaSuccess))
       ret = KVTC_ECUDA;
   }
   delete p;

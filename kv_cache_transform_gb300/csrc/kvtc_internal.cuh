@@ -7,7 +7,8 @@
 namespace kvtc {
 
 constexpr int kGroup = 16;         // components per microscaling group
-constexpr int kTileM = 128;        // tokens per tile (MMA M, TMEM lanes)
+constexpr int kTileM = 128;        // tokens per CTA tile (TMEM lanes)
+constexpr int kPairM = 256;        // tokens per CTA-pair super-tile (MMA M)
 constexpr int kAtomK = 64;         // 16-bit elements per 128-byte swizzle row
 constexpr int kMaxK = 240;         // kept components supported
 constexpr int kMaxRecord = 256;    // record bytes supported by the kernels
@@ -17,8 +18,8 @@ constexpr int kMaxD = 8192;
 // once by kvtc_calib_load and read by every kernel launch.
 struct DevStream {
   CUtensorMap tm_vdec;      // fp16 [D rows][kp cols]: V_kept, then mu_hi,
-                            // mu_lo and zeros (kp = k + 16), box {64, nc}
-  CUtensorMap tm_venc;      // bf16 V_kept as [k rows][D cols], box {64, k}
+                            // mu_lo and zeros (kp = k + 16), box {64, nc/2}
+  CUtensorMap tm_venc;      // bf16 V_kept as [k rows][D cols], box {64, k/2}
   const float* mu;          // [D]   fp32 mean
   const float* m;           // [k]   fp32 projection of the mean
   const uint8_t* bits;      // [Ga]  width of each active group
@@ -69,6 +70,8 @@ struct DecParams {
   int32_t nseg;
   int32_t total_tiles;
   int32_t tiles_per_seg;    // every stream of a call has the same T
+  int32_t nstages;          // B ring depth (shared-memory stages)
+  int32_t rec_words;        // record staging words per thread (max R / 4)
 };
 
 // Paged restore: work items are (request, stream, tile).
@@ -96,6 +99,8 @@ struct PagedParams {
   int32_t total_tiles;
   int32_t D;
   int64_t total_raw_chunks;
+  int32_t nstages;          // B ring depth (shared-memory stages)
+  int32_t rec_words;        // record staging words per thread (max R / 4)
 };
 
 // ---------------------------------------------------------------- raw rows
@@ -115,10 +120,14 @@ struct RawParams {
 };
 
 // Launchers (kvtc_kernels.cu).  Return a cudaError_t.
-cudaError_t launch_compress(const CompParams& p, int grid, cudaStream_t st);
-cudaError_t launch_decompress(const DecParams& p, int grid, cudaStream_t st);
-cudaError_t launch_decompress_paged(const PagedParams& p, int grid,
+// `pairs`: CTA pairs to launch (each kernel runs as clusters of two).
+cudaError_t launch_compress(const CompParams& p, int pairs, cudaStream_t st);
+cudaError_t launch_decompress(const DecParams& p, int pairs, cudaStream_t st);
+cudaError_t launch_decompress_paged(const PagedParams& p, int pairs,
                                     cudaStream_t st);
+// CTA pairs of each kernel that can be resident at once on this device.
+int max_pairs_compress(int smem_bytes);
+int max_pairs_decompress(int smem_bytes);
 cudaError_t launch_raw_copy(const RawParams& p, cudaStream_t st);
 cudaError_t launch_paged_raw(const PagedParams& p, cudaStream_t st);
 // Kernel launches issued by this library (all devices, all threads).
@@ -126,6 +135,9 @@ void count_launch();
 // CRC-32 of IEEE 802.3 (as zlib): reflected 0xEDB88320, init/final ~0.
 uint32_t crc32_ieee(const uint8_t* p, size_t n);
 int compress_smem_bytes(int nstages, int stage_bytes, int rec_stg_words);
-int decompress_smem_bytes();
+// Decompress shared memory for a ring of `nstages` and records of up to
+// 4 * rec_words bytes; decompress_stages picks the deepest ring that fits.
+int decompress_smem_bytes(int nstages, int rec_words);
+int decompress_stages(int rec_words);
 
 }  // namespace kvtc

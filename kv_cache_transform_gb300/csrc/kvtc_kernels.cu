@@ -28,7 +28,7 @@ namespace kvtc {
 // accumulates the SM cycles it spends in up to eight phases and lane 0
 // stores the sums per CTA.  Timestamps only; no work is skipped.
 #ifdef KVTC_TRACE
-__device__ unsigned long long g_kvtc_trace[2][160][16][8];
+__device__ unsigned long long g_kvtc_trace[2][160][32][8];
 #define KVTC_TR_DECL                              \
   unsigned long long tr_[8] = {0, 0, 0, 0, 0, 0, 0, 0}; \
   unsigned long long tr_t = clock64();
@@ -128,24 +128,28 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 // ======================================================================
 //                               decompress
 // ======================================================================
-constexpr int kDecWarps = 14;  // 0 TMA, 1 MMA, 2-5 prologue, 6-13 epilogue
+constexpr int kDecWarps = 18;  // 0 TMA, 1 MMA, 2-9 prologue, 10-17 epilogue
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kDecNC = 128;
-constexpr int kDecStages = 4;
-constexpr int kDecBStage = kDecNC * 128;           // [128 rows][64 fp16]
+constexpr int kDecMaxStages = 24;
+constexpr int kDecBStage = (kDecNC / 2) * 128;     // [64 rows][64 fp16]
 constexpr int kDecStgHalf = 32 * 128;             // 32 rows x 64 bf16, SW128
 constexpr int kDecStgWarp = 2 * kDecStgHalf;       // one 128-column chunk
-constexpr int kRecWords = kMaxRecord / 4;
-constexpr int kRecStgWarp = kRecWords * 33 * 4;    // [words][33] u32
-constexpr int kDecOffStg = kDecStages * kDecBStage;
-constexpr int kDecOffRec = kDecOffStg + 8 * kDecStgWarp;
-constexpr int kDecOffBar = kDecOffRec + 4 * kRecStgWarp;
-constexpr int kDecOffMisc = kDecOffBar + 256;
-constexpr int kDecSmem = kDecOffMisc + 64 + 1024;
+constexpr int kDecBarBytes = 512;
+// Shared memory: [B ring: nstages x 8 KB][staging: 8 warps x 8 KB]
+// [records: 8 warps x rec_words x 33 u32][barriers][misc]
+int decompress_smem_bytes(int nstages, int rec_words) {
+  return nstages * kDecBStage + 8 * kDecStgWarp + 8 * rec_words * 33 * 4 +
+         kDecBarBytes + 64 + 1024;
+}
+int decompress_stages(int rec_words) {
+  int n = kDecMaxStages;
+  while (n > 2 && decompress_smem_bytes(n, rec_words) > 232448) --n;
+  return n;
+}
 // TMEM columns: accumulators at 0 and 128, A operands at 256 and 384.
 constexpr uint32_t kDecTmemCols = 512;
 
-int decompress_smem_bytes() { return kDecSmem; }
 
 struct DecTile {
   const uint8_t* rec;  // record of compressed token 0 of the stream
@@ -180,7 +184,7 @@ __device__ __forceinline__ DecTile resolve(const PagedParams& p, int item) {
     if (p.tile_begin[mid] <= item) lo = mid; else hi = mid - 1;
   }
   const int r = lo;
-  const int tiles = max(1, (p.tc[r] + kTileM - 1) / kTileM);
+  const int tiles = max(1, (p.tc[r] + kPairM - 1) / kPairM);
   const int idx = item - p.tile_begin[r];
   const int j = idx / tiles;
   DecTile t;
@@ -221,49 +225,58 @@ __device__ __forceinline__ char* dec_row_ptr(const P& p, const DecTile& t,
 }
 
 template <class P>
-__global__ void __launch_bounds__(kDecThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
     decompress_kernel(const __grid_constant__ P p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
+  const int nst = p.nstages;
+  const int rec_words = p.rec_words;
   uint8_t* sB = smem;
-  uint8_t* sStg = smem + kDecOffStg;
-  uint32_t* sRec = reinterpret_cast<uint32_t*>(smem + kDecOffRec);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kDecOffBar);
-  uint64_t* full_b = bar;
-  uint64_t* empty_b = bar + 4;
-  uint64_t* a_full = bar + 8;
-  uint64_t* a_empty = bar + 10;
-  uint64_t* acc_full = bar + 12;
-  uint64_t* acc_empty = bar + 14;
-  uint64_t* mma_done = bar + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kDecOffMisc);
-  volatile int* abort_flag =
-      reinterpret_cast<volatile int*>(smem + kDecOffMisc + 4);
+  uint8_t* sStg = smem + nst * kDecBStage;
+  uint32_t* sRec = reinterpret_cast<uint32_t*>(sStg + 8 * kDecStgWarp);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(
+      reinterpret_cast<uint8_t*>(sRec) + 8 * rec_words * 33 * 4);
+  uint64_t* full_b = bar;                       // [nst], leader's used
+  uint64_t* empty_b = bar + kDecMaxStages;      // [nst]
+  uint64_t* a_full = bar + 2 * kDecMaxStages;   // [2], leader's used
+  uint64_t* a_empty = a_full + 2;               // [2]
+  uint64_t* acc_full = a_full + 4;              // [2]
+  uint64_t* acc_empty = a_full + 6;             // [2], leader's used
+  uint64_t* mma_done = a_full + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(
+      reinterpret_cast<uint8_t*>(bar) + kDecBarBytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // The CTA pair (a cluster of two) restores 256-token super-tiles: CTA
+  // `rank` owns rows [128 rank, 128 rank + 128) of each and the rank-th half
+  // of every V_dec chunk; the leader (rank 0) issues the M = 256 MMAs.
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kDecStages; ++i) {
+    for (int i = 0; i < nst; ++i) {
       mbar_init(&full_b[i], 1);
       mbar_init(&empty_b[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&a_full[i], 4);
+      mbar_init(&a_full[i], 8);      // 4 prologue warps in each CTA
       mbar_init(&a_empty[i], 1);
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4);
+      mbar_init(&acc_empty[i], 8);   // 4 epilogue warps in each CTA
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kDecTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, kDecTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int total = p.total_tiles;
@@ -272,29 +285,33 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     // ---------------------------------------------------- TMA producer
     if (lane == 0) {
       KVTC_TR_DECL
-      uint32_t it_b = 0;
+      uint32_t it_b = 0, s = 0, ph = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+      const uint32_t full_leader = mapa_shared(smem_u32(full_b), 0);
+      for (int item = pair; item < total && ok; item += npairs) {
         const DecTile t = resolve(p, item);
         const DevStream* ds = p.streams + t.cs;
-        const int nc = ds->nc, nch = ds->D / nc;
+        const int nc = ds->nc, nch = ds->D / nc, half = nc >> 1;
         const int nkb = (ds->kp + kAtomK - 1) / kAtomK;
-        const uint32_t bytes = (uint32_t)nc * 128u;
-        if (item == (int)blockIdx.x) prefetch_tmap(&ds->tm_vdec);
+        const uint32_t bytes_pair = (uint32_t)nc * 128u;  // both halves
+        if (item == pair) prefetch_tmap(&ds->tm_vdec);
         for (int ch = 0; ch < nch && ok; ++ch) {
           for (int kb = 0; kb < nkb; ++kb) {
-            const uint32_t s = it_b & (kDecStages - 1);
-            const uint32_t ph = (it_b / kDecStages) & 1u;
             KVTC_TR(0)
             if (!mbar_wait(&empty_b[s], ph ^ 1u, abort_flag)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&full_b[s], bytes);
+            if (leader) mbar_arrive_expect_tx(&full_b[s], bytes_pair);
             KVTC_TR(1)
-            tma_load_2d(sB + s * kDecBStage, &ds->tm_vdec, kb * kAtomK,
-                        ch * nc, &full_b[s]);
+            tma_load_2d_pair(sB + s * kDecBStage, &ds->tm_vdec, kb * kAtomK,
+                             ch * nc + (int)rank * half,
+                             full_leader + s * 8u);
             ++it_b;
+            if (++s == (uint32_t)nst) {
+              s = 0;
+              ph ^= 1u;
+            }
             KVTC_TR(2)
           }
         }
@@ -302,27 +319,30 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       KVTC_TR(0)
       KVTC_TR_SAVE(0)
       if (!ok) raise_abort(abort_flag, p.status);
-      for (uint32_t s = 0; s < kDecStages; ++s) {
-        if (it_b > s) {
-          const uint32_t last = s + kDecStages * ((it_b - 1 - s) / kDecStages);
-          mbar_drain(&full_b[s], (last / kDecStages) & 1u);
+      if (leader) {
+        // the leader's full barriers count both CTAs' loads
+        for (uint32_t s2 = 0; s2 < (uint32_t)nst; ++s2) {
+          if (it_b > s2) {
+            const uint32_t last = s2 + nst * ((it_b - 1 - s2) / nst);
+            mbar_drain(&full_b[s2], (last / nst) & 1u);
+          }
         }
       }
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // ---------------------------------------------- MMA issuer (leader)
+    if (lane == 0 && leader) {
       KVTC_TR_DECL
-      uint32_t it_b = 0, chunk = 0, it = 0;
+      uint32_t chunk = 0, it = 0, s = 0, ph = 0;
       bool ok = true;
       const uint64_t desc_b0 = sw128_desc(smem_u32(sB));
-      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+      for (int item = pair; item < total && ok; item += npairs) {
         const DecTile t = resolve(p, item);
         const DevStream* ds = p.streams + t.cs;
         const int nc = ds->nc, nch = ds->D / nc;
         const int nkb = (ds->kp + kAtomK - 1) / kAtomK;
         const int ksteps = ds->kp / kGroup;  // kept groups + the mean step
-        const uint32_t idesc = make_idesc(128, (uint32_t)nc, 0);
+        const uint32_t idesc = make_idesc(256, (uint32_t)nc, 0);
         const uint32_t abuf = it & 1u;
         KVTC_TR(0)
         if (!mbar_wait(&a_full[abuf], (it >> 1) & 1u, abort_flag)) {
@@ -345,10 +365,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           const uint32_t d = tmem + accb * 128u;
           uint32_t acol = a_col;
           for (int kb = 0; kb < nkb; ++kb) {
-            const uint32_t s = it_b & (kDecStages - 1);
             KVTC_TR(0)
-            if (!mbar_wait(&full_b[s], (it_b / kDecStages) & 1u,
-                           abort_flag)) {
+            if (!mbar_wait(&full_b[s], ph, abort_flag)) {
               ok = false;
               break;
             }
@@ -357,55 +375,57 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             // descriptor start address advances 32 bytes (2 units) per K=16
             const uint64_t bdesc = desc_b0 + (uint64_t)(s * (kDecBStage >> 4));
             const int nks = min(4, ksteps - kb * 4);
-            mma_ts(d, acol, bdesc, idesc, kb > 0);
-            if (nks > 1) mma_ts(d, acol + 8u, bdesc + 2u, idesc, 1u);
-            if (nks > 2) mma_ts(d, acol + 16u, bdesc + 4u, idesc, 1u);
-            if (nks > 3) mma_ts(d, acol + 24u, bdesc + 6u, idesc, 1u);
+            mma_ts_pair(d, acol, bdesc, idesc, kb > 0);
+            if (nks > 1) mma_ts_pair(d, acol + 8u, bdesc + 2u, idesc, 1u);
+            if (nks > 2) mma_ts_pair(d, acol + 16u, bdesc + 4u, idesc, 1u);
+            if (nks > 3) mma_ts_pair(d, acol + 24u, bdesc + 6u, idesc, 1u);
             acol += 32u;
-            tc_commit(&empty_b[s]);
-            ++it_b;
+            tc_commit_pair(&empty_b[s], 3);
+            if (++s == (uint32_t)nst) {
+              s = 0;
+              ph ^= 1u;
+            }
             KVTC_TR(4)
           }
           if (!ok) break;
-          tc_commit(&acc_full[accb]);
+          tc_commit_pair(&acc_full[accb], 3);
           ++chunk;
         }
         if (!ok) break;
-        tc_commit(&a_empty[abuf]);
+        tc_commit_pair(&a_empty[abuf], 3);
         ++it;
       }
       KVTC_TR(0)
       KVTC_TR_SAVE(0)
       if (!ok) raise_abort(abort_flag, p.status);
-      tc_commit(mma_done);
-      mbar_drain(mma_done, 0);
+      tc_commit_pair(mma_done, 3);
     }
+    if (lane == 0) mbar_drain(mma_done, 0);
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < 10) {
     // ------------------------------------ prologue: unpack + dequantise
+    // Two sets of four warps (one per TMEM lane quadrant each): set 0 builds
+    // the A operand of the even super-tiles (buffer 0), set 1 of the odd.
     const int q = warp & 3;
-    uint32_t* stg = sRec + (warp - 2) * (kRecWords * 33);
+    const uint32_t set = (uint32_t)(warp - 2) >> 2;
+    uint32_t* stg = sRec + (warp - 2) * (rec_words * 33);
+    const uint32_t a_full_leader = mapa_shared(smem_u32(a_full), 0);
     uint32_t it = 0;
     bool ok = true;
     KVTC_TR_DECL
-    for (int item = blockIdx.x; item < total; item += gridDim.x) {
+    for (int item = pair; item < total; item += npairs, ++it) {
+      const uint32_t abuf = it & 1u;
+      if (abuf != set) continue;
       const DecTile t = resolve(p, item);
       const DevStream* ds = p.streams + t.cs;
       const int R = ds->R, Ga = ds->Ga;
-      const uint32_t abuf = it & 1u;
-      KVTC_TR(0)
-      if (!mbar_wait(&a_empty[abuf], ((it >> 1) & 1u) ^ 1u, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      KVTC_TR(1)
-      const int row0 = t.tile * kTileM + q * 32;
+      const int row0 = t.tile * kPairM + (int)rank * kTileM + q * 32;
       const int nvalid = min(max(t.tc - row0, 0), 32);
       const uint8_t* rbase = t.rec + (int64_t)row0 * R;
       // Coalesced 16-byte loads of the warp's 32 records (up to eight in
       // flight per lane), stored word-transposed ([word][token], row pitch
-      // 33) in shared memory.
+      // 33) in shared memory; done before waiting for the A buffer so the
+      // memory latency overlaps the MMAs still reading it.
       const int nld = (32 * R) >> 9;  // 16-byte loads per lane
       for (int b0 = 0; b0 < nld; b0 += 8) {
         uint4 v[8];
@@ -427,6 +447,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           stg[(wd + 3) * 33 + tr] = v[u].w;
         }
       }
+      KVTC_TR(2)
+      if (!mbar_wait(&a_empty[abuf], ((it >> 1) & 1u) ^ 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      KVTC_TR(1)
       __syncwarp();
       KVTC_TR(2)
       const uint32_t a_tmem =
@@ -469,8 +496,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&a_full[abuf]);
-      ++it;
+      if (lane == 0) mbar_arrive_cluster(a_full_leader + abuf * 8u);
       KVTC_TR(4)
     }
     KVTC_TR(0)
@@ -485,18 +511,20 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     // coalesced 16-byte stores through the block table (paged output).
     constexpr bool kPaged = std::is_same<P, PagedParams>::value;
     const int q = warp & 3;
-    const uint32_t set = (uint32_t)(warp - 6) >> 2;
-    uint8_t* stg_w = sStg + (warp - 6) * kDecStgWarp;
+    const uint32_t set = (uint32_t)(warp - 10) >> 2;
+    uint8_t* stg_w = sStg + (warp - 10) * kDecStgWarp;
     const uint32_t stg_row = smem_u32(stg_w) + lane * 128;
     const uint32_t sw = (uint32_t)(lane & 7);
+    const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
     uint32_t chunk = 0;
     bool ok = true;
     KVTC_TR_DECL
-    for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+    for (int item = pair; item < total && ok; item += npairs) {
       const DecTile t = resolve(p, item);
       const DevStream* ds = p.streams + t.cs;
       const int D = ds->D, nc = ds->nc, nch = D / nc;
-      const int row = t.tile * kTileM + q * 32 + lane;
+      const int wrow0 = t.tile * kPairM + (int)rank * kTileM + q * 32;
+      const int row = wrow0 + lane;
       char* rowp = nullptr;
       if constexpr (kPaged) {
         if (row < t.tc) rowp = dec_row_ptr(p, t, row, D);
@@ -517,20 +545,22 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         KVTC_TR(1)
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + accb * 128u;
         const int npc = nc / 32;
-        for (int pc = 0; pc < npc; pc += 2) {
-          float v[64];
+        for (int pc = 0; pc < npc; ++pc) {
+          float v[32];
           tmem_ld32(taddr + (uint32_t)pc * 32u, v);
-          tmem_ld32(taddr + (uint32_t)(pc + 1) * 32u, v + 32);
           tmem_wait_ld();
-          if (pc + 2 >= npc) {
+          if (pc + 1 == npc) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[accb]);
+            if (lane == 0) mbar_arrive_cluster(acc_empty_leader + accb * 8u);
           }
-          const uint32_t half = stg_row + (uint32_t)(pc >> 1) * kDecStgHalf;
+          // 32 columns = 4 of the 8 16-byte chunks of a 64-column box row
+          const uint32_t hf = stg_row + (uint32_t)(pc >> 1) * kDecStgHalf;
+          const uint32_t c0 = (uint32_t)(pc & 1) * 4u;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            sts_v4(half + ((i ^ sw) << 4), pack_bf16(v[8 * i], v[8 * i + 1]),
+          for (int i = 0; i < 4; ++i)
+            sts_v4(hf + (((c0 + i) ^ sw) << 4),
+                   pack_bf16(v[8 * i], v[8 * i + 1]),
                    pack_bf16(v[8 * i + 2], v[8 * i + 3]),
                    pack_bf16(v[8 * i + 4], v[8 * i + 5]),
                    pack_bf16(v[8 * i + 6], v[8 * i + 7]));
@@ -539,12 +569,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if constexpr (!kPaged) {
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) {
+          if (lane == 0 && wrow0 < t.tc) {
             for (int h = 0; h < nc / 64; ++h)
-              tma_store_2d(&p.tm_out[t.seg], ch * nc + h * 64,
-                           t.tile * kTileM + q * 32, stg_w + h * kDecStgHalf);
-            bulk_commit();
+              tma_store_2d(&p.tm_out[t.seg], ch * nc + h * 64, wrow0,
+                           stg_w + h * kDecStgHalf);
           }
+          if (lane == 0) bulk_commit();
         } else {
           __syncwarp();
           // a row chunk (nc * 2 bytes) is written by nc / 8 lanes, 16 bytes
@@ -576,14 +606,16 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     if (!ok && lane == 0) raise_abort(abort_flag, p.status);
   }
 
+  // No CTA of the pair may leave while the other can still reach its
+  // barriers, shared memory or TMEM.
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kDecTmemCols);
+    tmem_dealloc_pair(tmem, kDecTmemCols);
   }
+  cluster_sync();
 }
-
 // ======================================================================
 //                                compress
 // ======================================================================
@@ -601,7 +633,7 @@ __device__ __forceinline__ int find_comp_seg(const CompParams& p, int item) {
   return item / p.tiles_per_seg;
 }
 
-__global__ void __launch_bounds__(kCompThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
     compress_kernel(const __grid_constant__ CompParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -621,6 +653,12 @@ __global__ void __launch_bounds__(kCompThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // The CTA pair (a cluster of two) codes 256-token super-tiles: CTA `rank`
+  // loads rows [128 rank, 128 rank + 128) and the rank-th half of V_enc's
+  // components; the leader (rank 0) issues the M = 256 MMAs.
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < nst; ++i) {
@@ -629,18 +667,18 @@ __global__ void __launch_bounds__(kCompThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4);
+      mbar_init(&acc_empty[i], 8);   // 4 epilogue warps in each CTA
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kCompTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, kCompTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int total = p.total_tiles;
@@ -651,13 +689,17 @@ __global__ void __launch_bounds__(kCompThreads, 1)
       KVTC_TR_DECL
       uint32_t it_b = 0, s = 0, ph = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+      const uint32_t full_leader = mapa_shared(smem_u32(full), 0);
+      for (int item = pair; item < total && ok; item += npairs) {
         const int sg = find_comp_seg(p, item);
         const CompSeg& g = p.seg[sg];
         const int tile = item - sg * p.tiles_per_seg;
         const DevStream* ds = p.streams + g.cs;
         const int nkb = ds->D / kAtomK;
-        const uint32_t bytes = (uint32_t)kCompAStage + (uint32_t)ds->k * 128u;
+        const int half = ds->k >> 1;
+        // both CTAs' A tiles and B halves land on the leader's barrier
+        const uint32_t bytes_pair =
+            2u * ((uint32_t)kCompAStage + (uint32_t)half * 128u);
         for (int kb = 0; kb < nkb; ++kb) {
           KVTC_TR(0)
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) {
@@ -666,10 +708,12 @@ __global__ void __launch_bounds__(kCompThreads, 1)
           }
           KVTC_TR(1)
           uint8_t* st = smem + s * stage_bytes;
-          mbar_arrive_expect_tx(&full[s], bytes);
-          tma_load_2d(st, &g.tm_x, kb * kAtomK, g.row0 + tile * kTileM,
-                      &full[s]);
-          tma_load_2d(st + kCompAStage, &ds->tm_venc, kb * kAtomK, 0, &full[s]);
+          if (leader) mbar_arrive_expect_tx(&full[s], bytes_pair);
+          tma_load_2d_pair(st, &g.tm_x, kb * kAtomK,
+                           g.row0 + tile * kPairM + (int)rank * kTileM,
+                           full_leader + s * 8u);
+          tma_load_2d_pair(st + kCompAStage, &ds->tm_venc, kb * kAtomK,
+                           (int)rank * half, full_leader + s * 8u);
           ++it_b;
           if (++s == (uint32_t)nst) {
             s = 0;
@@ -681,27 +725,30 @@ __global__ void __launch_bounds__(kCompThreads, 1)
       KVTC_TR(0)
       KVTC_TR_SAVE(1)
       if (!ok) raise_abort(abort_flag, p.status);
-      for (uint32_t s = 0; s < (uint32_t)nst; ++s) {
-        if (it_b > s) {
-          const uint32_t last = s + nst * ((it_b - 1 - s) / nst);
-          mbar_drain(&full[s], (last / nst) & 1u);
+      if (leader) {
+        // the leader's full barriers count both CTAs' loads
+        for (uint32_t s = 0; s < (uint32_t)nst; ++s) {
+          if (it_b > s) {
+            const uint32_t last = s + nst * ((it_b - 1 - s) / nst);
+            mbar_drain(&full[s], (last / nst) & 1u);
+          }
         }
       }
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // ---------------------------------------------- MMA issuer (leader)
+    if (lane == 0 && leader) {
       KVTC_TR_DECL
       uint32_t it = 0, s = 0, ph = 0;
       bool ok = true;
       const uint64_t desc_s0 = sw128_desc(smem_u32(smem));
       const uint64_t stage_units = (uint64_t)(stage_bytes >> 4);
       const uint64_t b_units = (uint64_t)(kCompAStage >> 4);
-      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+      for (int item = pair; item < total && ok; item += npairs) {
         const CompSeg& g = p.seg[find_comp_seg(p, item)];
         const DevStream* ds = p.streams + g.cs;
         const int nkb = ds->D / kAtomK;
-        const uint32_t idesc = make_idesc(128, (uint32_t)ds->k, 1);
+        const uint32_t idesc = make_idesc(256, (uint32_t)ds->k, 1);
         const uint32_t accb = it & 1u;
         KVTC_TR(0)
         if (!mbar_wait(&acc_empty[accb], ((it >> 1) & 1u) ^ 1u, abort_flag)) {
@@ -721,11 +768,11 @@ __global__ void __launch_bounds__(kCompThreads, 1)
           KVTC_TR(2)
           const uint64_t ad = desc_s0 + s * stage_units;
           const uint64_t bd = ad + b_units;
-          mma_ss(d, ad, bd, idesc, kb > 0);
-          mma_ss(d, ad + 2u, bd + 2u, idesc, 1u);
-          mma_ss(d, ad + 4u, bd + 4u, idesc, 1u);
-          mma_ss(d, ad + 6u, bd + 6u, idesc, 1u);
-          tc_commit(&empty[s]);
+          mma_ss_pair(d, ad, bd, idesc, kb > 0);
+          mma_ss_pair(d, ad + 2u, bd + 2u, idesc, 1u);
+          mma_ss_pair(d, ad + 4u, bd + 4u, idesc, 1u);
+          mma_ss_pair(d, ad + 6u, bd + 6u, idesc, 1u);
+          tc_commit_pair(&empty[s], 3);
           if (++s == (uint32_t)nst) {
             s = 0;
             ph ^= 1u;
@@ -733,15 +780,15 @@ __global__ void __launch_bounds__(kCompThreads, 1)
           KVTC_TR(3)
         }
         if (!ok) break;
-        tc_commit(&acc_full[accb]);
+        tc_commit_pair(&acc_full[accb], 3);
         ++it;
       }
       KVTC_TR(0)
       KVTC_TR_SAVE(1)
       if (!ok) raise_abort(abort_flag, p.status);
-      tc_commit(mma_done);
-      mbar_drain(mma_done, 0);
+      tc_commit_pair(mma_done, 3);
     }
+    if (lane == 0) mbar_drain(mma_done, 0);
     __syncwarp();
   } else {
     // ------------------------- epilogue: quantise + bit-plane records
@@ -751,10 +798,11 @@ __global__ void __launch_bounds__(kCompThreads, 1)
     const uint32_t set = (uint32_t)(warp - 2) >> 2;
     uint32_t* stg = sRec + (warp - 2) * (rec_words * 33);
     const uint32_t stg_addr = smem_u32(stg);
+    const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
     uint32_t it = 0;
     bool ok = true;
     KVTC_TR_DECL
-    for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
+    for (int item = pair; item < total; item += npairs, ++it) {
       const uint32_t accb = it & 1u;
       if (accb != set) continue;
       const int sg = find_comp_seg(p, item);
@@ -769,7 +817,7 @@ __global__ void __launch_bounds__(kCompThreads, 1)
       }
       tc_fence_after();
       KVTC_TR(1)
-      const int row0 = tile * kTileM + q * 32;
+      const int row0 = tile * kPairM + (int)rank * kTileM + q * 32;
       const int nvalid = min(max(g.tc - row0, 0), 32);
       for (int w = 0; w < (R >> 2); ++w) stg[w * 33 + lane] = 0u;
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + accb * 256u;
@@ -783,7 +831,7 @@ __global__ void __launch_bounds__(kCompThreads, 1)
         if (a0 + 2 >= Ga) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[accb]);
+          if (lane == 0) mbar_arrive_cluster(acc_empty_leader + accb * 8u);
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -864,12 +912,15 @@ __global__ void __launch_bounds__(kCompThreads, 1)
     if (!ok && lane == 0) raise_abort(abort_flag, p.status);
   }
 
+  // No CTA of the pair may leave while the other can still reach its
+  // barriers, shared memory or TMEM.
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kCompTmemCols);
+    tmem_dealloc_pair(tmem, kCompTmemCols);
   }
+  cluster_sync();
 }
 
 // ======================================================================
@@ -950,42 +1001,71 @@ extern "C" int kvtc_trace_read(void* host, size_t bytes) {
 namespace kvtc {
 #endif
 
-cudaError_t launch_compress(const CompParams& p, int grid, cudaStream_t st) {
-  const int smem = compress_smem_bytes(p.nstages, p.stage_bytes, p.rec_stg_words);
-  static int configured = 0;
-  if (configured < smem) {
-    cudaError_t e = cudaFuncSetAttribute(
-        compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-    if (e != cudaSuccess) return e;
-    configured = 232448;
+static int max_pairs(const void* func, int threads, int smem) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, func, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return sms / 2;
   }
-  compress_kernel<<<grid, kCompThreads, smem, st>>>(p);
+  return n;
+}
+
+static void allow_smem(const void* func, int bytes) {
+  cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       bytes);
+}
+
+int max_pairs_compress(int smem_bytes) {
+  allow_smem((const void*)compress_kernel, 232448);
+  return max_pairs((const void*)compress_kernel, kCompThreads, smem_bytes);
+}
+
+int max_pairs_decompress(int smem_bytes) {
+  allow_smem((const void*)decompress_kernel<DecParams>, 232448);
+  allow_smem((const void*)decompress_kernel<PagedParams>, 232448);
+  return max_pairs((const void*)decompress_kernel<DecParams>, kDecThreads,
+                   smem_bytes);
+}
+
+cudaError_t launch_compress(const CompParams& p, int pairs, cudaStream_t st) {
+  const int smem = compress_smem_bytes(p.nstages, p.stage_bytes, p.rec_stg_words);
+  allow_smem((const void*)compress_kernel, 232448);
+  compress_kernel<<<2 * pairs, kCompThreads, smem, st>>>(p);
   count_launch();
   return cudaGetLastError();
 }
 
 template <class P>
-static cudaError_t launch_dec(const P& p, int grid, cudaStream_t st) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(
-        decompress_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        kDecSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  decompress_kernel<P><<<grid, kDecThreads, kDecSmem, st>>>(p);
+static cudaError_t launch_dec(const P& p, int pairs, cudaStream_t st) {
+  allow_smem((const void*)decompress_kernel<P>, 232448);
+  decompress_kernel<P><<<2 * pairs, kDecThreads,
+                         decompress_smem_bytes(p.nstages, p.rec_words), st>>>(
+      p);
   count_launch();
   return cudaGetLastError();
 }
 
-cudaError_t launch_decompress(const DecParams& p, int grid, cudaStream_t st) {
-  return launch_dec(p, grid, st);
+cudaError_t launch_decompress(const DecParams& p, int pairs, cudaStream_t st) {
+  return launch_dec(p, pairs, st);
 }
 
-cudaError_t launch_decompress_paged(const PagedParams& p, int grid,
+cudaError_t launch_decompress_paged(const PagedParams& p, int pairs,
                                     cudaStream_t st) {
-  return launch_dec(p, grid, st);
+  return launch_dec(p, pairs, st);
 }
 
 cudaError_t launch_raw_copy(const RawParams& p, cudaStream_t st) {
