@@ -138,6 +138,22 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base,
   return r == CUDA_SUCCESS;
 }
 
+// V_dec, K-block major [nkb][D][64] fp16: box {64, rows, nkb}, 128-byte
+// swizzle; the box lands in shared memory as nkb [rows][64] tiles.
+bool encode_vdec_3d(CUtensorMap* m, const void* base, uint64_t D,
+                    uint64_t nkb, uint32_t rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {64, D, nkb};
+  cuuint64_t strides[2] = {128, 128ull * D};
+  cuuint32_t box[3] = {64u, rows, (cuuint32_t)nkb};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base),
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Output map for the reconstruction epilogue: bf16 rows [rows][cols] with a
 // stride of row_bytes, box {64 columns, 32 rows}, 128-byte swizzle.
 bool encode_store_2d(CUtensorMap* m, const void* base, uint64_t cols,
@@ -377,7 +393,8 @@ int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
     o.bits = total; total = align_up(total + h.Ga, 256);
     o.poff = total; total = align_up(total + 2LL * h.Ga, 256);
     o.venc = total; total = align_up(total + 2LL * h.k * h.D, 256);
-    o.vdec = total; total = align_up(total + 2LL * (h.k + 16) * h.D, 256);
+    o.vdec = total;
+    total = align_up(total + 2LL * ((h.k + 16 + 63) / 64 * 64) * h.D, 256);
   }
   std::vector<uint8_t> host((size_t)total, 0);
   if (cudaMalloc(&c->pool, (size_t)total) != cudaSuccess) {
@@ -399,6 +416,11 @@ int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
     uint16_t* vdec = reinterpret_cast<uint16_t*>(host.data() + o.vdec);
     std::vector<double> muv(h.D);
     const int kp = h.k + 16;
+    // V_dec is stored K-block major, [kb][d][64], so that one 3-D TMA box
+    // brings all K blocks of a run of output channels
+    auto vd = [&](int d, int col) -> uint16_t& {
+      return vdec[((size_t)(col >> 6) * h.D + d) * 64 + (col & 63)];
+    };
     for (int d = 0; d < h.D; ++d) {
       std::memcpy(&muv[d], mu + d, 8);
       hmu[d] = (float)muv[d];
@@ -407,8 +429,8 @@ int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
       // holds 1.0 there), the other 14 columns of that step are zero
       const uint16_t hi = fp16_bits_rne(muv[d]);
       const double hiv = (double)__half2float(__ushort_as_half(hi));
-      vdec[(size_t)d * kp + h.k] = hi;
-      vdec[(size_t)d * kp + h.k + 1] = fp16_bits_rne(muv[d] - hiv);
+      vd(d, h.k) = hi;
+      vd(d, h.k + 1) = fp16_bits_rne(muv[d] - hiv);
     }
     for (int a = 0; a < h.k; ++a) {
       double acc = 0.0;
@@ -417,7 +439,7 @@ int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
         std::memcpy(&v, V + (size_t)a * h.D + d, 8);
         const uint16_t eb = bf16_bits_rne(v);
         venc[(size_t)a * h.D + d] = eb;
-        vdec[(size_t)d * kp + a] = fp16_bits_rne(v);
+        vd(d, a) = fp16_bits_rne(v);
         uint32_t u = (uint32_t)eb << 16;
         float ef;
         std::memcpy(&ef, &u, 4);
@@ -448,10 +470,10 @@ int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
     s.R = h.R;
     s.nc = (h.D % 128 == 0) ? 128 : 64;
     s.kp = kp;
-    // each CTA of a pair loads half of the N rows of the B operand
-    if (!encode_2d(&s.tm_vdec, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, dev + o.vdec,
-                   (uint64_t)kp, (uint64_t)h.D, 2ull * kp,
-                   (uint32_t)(s.nc / 2)) ||
+    // each CTA of a pair loads half of the N rows of the B operand, all K
+    // blocks at once
+    if (!encode_vdec_3d(&s.tm_vdec, dev + o.vdec, (uint64_t)h.D,
+                        (uint64_t)((kp + 63) / 64), (uint32_t)(s.nc / 2)) ||
         !encode_2d(&s.tm_venc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dev + o.venc,
                    (uint64_t)h.D, (uint64_t)h.k, 2ull * h.D,
                    (uint32_t)(h.k / 2))) {

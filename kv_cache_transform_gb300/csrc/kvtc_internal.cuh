@@ -17,8 +17,9 @@ constexpr int kMaxD = 8192;
 // Device-resident description of one calibrated (layer, K|V) stream; built
 // once by kvtc_calib_load and read by every kernel launch.
 struct DevStream {
-  CUtensorMap tm_vdec;      // fp16 [D rows][kp cols]: V_kept, then mu_hi,
-                            // mu_lo and zeros (kp = k + 16), box {64, nc/2}
+  CUtensorMap tm_vdec;      // fp16 [kb][D][64]: V_kept, then mu_hi, mu_lo,
+                            // zeros (kp = k + 16 columns, padded to 64s),
+                            // box {64, nc/2, kb}
   CUtensorMap tm_venc;      // bf16 V_kept as [k rows][D cols], box {64, k/2}
   const float* mu;          // [D]   fp32 mean
   const float* m;           // [k]   fp32 projection of the mean

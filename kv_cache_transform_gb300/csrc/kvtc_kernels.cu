@@ -131,8 +131,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 constexpr int kDecWarps = 18;  // 0 TMA, 1 MMA, 2-9 prologue, 10-17 epilogue
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kDecNC = 128;
-constexpr int kDecMaxStages = 24;
-constexpr int kDecBStage = (kDecNC / 2) * 128;     // [64 rows][64 fp16]
+constexpr int kDecMaxStages = 8;
+// one B stage = this CTA's half of a chunk, every K block: [kb][64 rows][64]
+constexpr int kDecBStage = (kDecNC / 2) * 128 * (kMaxK / 64 + 1);
 constexpr int kDecStgHalf = 32 * 128;             // 32 rows x 64 bf16, SW128
 constexpr int kDecStgWarp = 2 * kDecStgHalf;       // one 128-column chunk
 constexpr int kDecBarBytes = 512;
@@ -265,7 +266,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       mbar_init(&a_full[i], 8);      // 4 prologue warps in each CTA
       mbar_init(&a_empty[i], 1);
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 8);   // 4 epilogue warps in each CTA
+      mbar_init(&acc_empty[i], 16);  // 8 epilogue warps in each CTA
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -293,27 +294,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         const DevStream* ds = p.streams + t.cs;
         const int nc = ds->nc, nch = ds->D / nc, half = nc >> 1;
         const int nkb = (ds->kp + kAtomK - 1) / kAtomK;
-        const uint32_t bytes_pair = (uint32_t)nc * 128u;  // both halves
+        // both halves of the chunk, every K block
+        const uint32_t bytes_pair = (uint32_t)nc * 128u * (uint32_t)nkb;
         if (item == pair) prefetch_tmap(&ds->tm_vdec);
-        for (int ch = 0; ch < nch && ok; ++ch) {
-          for (int kb = 0; kb < nkb; ++kb) {
-            KVTC_TR(0)
-            if (!mbar_wait(&empty_b[s], ph ^ 1u, abort_flag)) {
-              ok = false;
-              break;
-            }
-            if (leader) mbar_arrive_expect_tx(&full_b[s], bytes_pair);
-            KVTC_TR(1)
-            tma_load_2d_pair(sB + s * kDecBStage, &ds->tm_vdec, kb * kAtomK,
-                             ch * nc + (int)rank * half,
-                             full_leader + s * 8u);
-            ++it_b;
-            if (++s == (uint32_t)nst) {
-              s = 0;
-              ph ^= 1u;
-            }
-            KVTC_TR(2)
+        for (int ch = 0; ch < nch; ++ch) {
+          KVTC_TR(0)
+          if (!mbar_wait(&empty_b[s], ph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
           }
+          if (leader) mbar_arrive_expect_tx(&full_b[s], bytes_pair);
+          KVTC_TR(1)
+          tma_load_3d_pair(sB + s * kDecBStage, &ds->tm_vdec, 0,
+                           ch * nc + (int)rank * half, 0,
+                           full_leader + s * 8u);
+          ++it_b;
+          if (++s == (uint32_t)nst) {
+            s = 0;
+            ph ^= 1u;
+          }
+          KVTC_TR(2)
         }
       }
       KVTC_TR(0)
@@ -340,8 +340,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         const DecTile t = resolve(p, item);
         const DevStream* ds = p.streams + t.cs;
         const int nc = ds->nc, nch = ds->D / nc;
-        const int nkb = (ds->kp + kAtomK - 1) / kAtomK;
         const int ksteps = ds->kp / kGroup;  // kept groups + the mean step
+        const int kb_units = (ds->nc / 2) * 128 / 16;  // one K block, >> 4
         const uint32_t idesc = make_idesc(256, (uint32_t)nc, 0);
         const uint32_t abuf = it & 1u;
         KVTC_TR(0)
@@ -363,30 +363,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
           tc_fence_after();
           KVTC_TR(2)
           const uint32_t d = tmem + accb * 128u;
-          uint32_t acol = a_col;
-          for (int kb = 0; kb < nkb; ++kb) {
-            KVTC_TR(0)
-            if (!mbar_wait(&full_b[s], ph, abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            KVTC_TR(3)
-            // descriptor start address advances 32 bytes (2 units) per K=16
-            const uint64_t bdesc = desc_b0 + (uint64_t)(s * (kDecBStage >> 4));
-            const int nks = min(4, ksteps - kb * 4);
-            mma_ts_pair(d, acol, bdesc, idesc, kb > 0);
-            if (nks > 1) mma_ts_pair(d, acol + 8u, bdesc + 2u, idesc, 1u);
-            if (nks > 2) mma_ts_pair(d, acol + 16u, bdesc + 4u, idesc, 1u);
-            if (nks > 3) mma_ts_pair(d, acol + 24u, bdesc + 6u, idesc, 1u);
-            acol += 32u;
-            tc_commit_pair(&empty_b[s], 3);
-            if (++s == (uint32_t)nst) {
-              s = 0;
-              ph ^= 1u;
-            }
-            KVTC_TR(4)
+          KVTC_TR(0)
+          if (!mbar_wait(&full_b[s], ph, abort_flag)) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
+          KVTC_TR(3)
+          // K block kb of this CTA's half lies at kb * half * 128 bytes; the
+          // descriptor start address advances 32 bytes (2 units) per K=16
+          const uint64_t bdesc = desc_b0 + (uint64_t)(s * (kDecBStage >> 4));
+          for (int step = 0; step < ksteps; ++step)
+            mma_ts_pair(d, a_col + (uint32_t)step * 8u,
+                        bdesc + (uint64_t)((step >> 2) * kb_units +
+                                           (step & 3) * 2),
+                        idesc, step > 0);
+          tc_commit_pair(&empty_b[s], 3);
+          if (++s == (uint32_t)nst) {
+            s = 0;
+            ph ^= 1u;
+          }
+          KVTC_TR(4)
           if (!ok) break;
           tc_commit_pair(&acc_full[accb], 3);
           ++chunk;
@@ -504,16 +501,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
     if (!ok && lane == 0) raise_abort(abort_flag, p.status);
   } else {
     // -------------- epilogue: bf16 rows (the mean came in the MMA)
-    // Two sets of four warps (one per TMEM lane quadrant each): set 0
-    // drains the even chunks (accumulator 0), set 1 the odd ones.  A warp
-    // stages its 32 rows x 128 columns as two 128-byte-swizzled boxes and
-    // writes them with TMA tensor stores (contiguous output) or with
-    // coalesced 16-byte stores through the block table (paged output).
+    // Two sets of four warps (one per TMEM lane quadrant each) share every
+    // chunk: set h takes its columns [64 h, 64 h + 64), so an accumulator
+    // is released after one TMEM round trip.  A warp stages its 32 rows x
+    // 64 columns as one 128-byte-swizzled box (two boxes alternate between
+    // chunks) and writes it with a TMA tensor store (contiguous output) or
+    // with coalesced 16-byte stores through the block table (paged).
     constexpr bool kPaged = std::is_same<P, PagedParams>::value;
     const int q = warp & 3;
-    const uint32_t set = (uint32_t)(warp - 10) >> 2;
-    uint8_t* stg_w = sStg + (warp - 10) * kDecStgWarp;
-    const uint32_t stg_row = smem_u32(stg_w) + lane * 128;
+    const int col0 = ((warp - 10) >> 2) * 64;
+    uint8_t* stg_base = sStg + (warp - 10) * kDecStgWarp;
     const uint32_t sw = (uint32_t)(lane & 7);
     const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
     uint32_t chunk = 0;
@@ -523,77 +520,71 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       const DecTile t = resolve(p, item);
       const DevStream* ds = p.streams + t.cs;
       const int D = ds->D, nc = ds->nc, nch = D / nc;
+      const bool mine = col0 < nc;
       const int wrow0 = t.tile * kPairM + (int)rank * kTileM + q * 32;
       const int row = wrow0 + lane;
       char* rowp = nullptr;
       if constexpr (kPaged) {
-        if (row < t.tc) rowp = dec_row_ptr(p, t, row, D);
+        if (mine && row < t.tc) rowp = dec_row_ptr(p, t, row, D);
       }
       for (int ch = 0; ch < nch; ++ch, ++chunk) {
         const uint32_t accb = chunk & 1u;
-        if (accb != set) continue;
         KVTC_TR(0)
         if (!mbar_wait(&acc_full[accb], (chunk >> 1) & 1u, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        KVTC_TR(1)
+        float v[64];
+        if (mine) {
+          const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) +
+                                 accb * 128u + (uint32_t)col0;
+          tmem_ld32(taddr, v);
+          tmem_ld32(taddr + 32u, v + 32);
+          tmem_wait_ld();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty_leader + accb * 8u);
+        if (!mine) continue;
+        uint8_t* stg_w = stg_base + (chunk & 1u) * kDecStgHalf;
         if constexpr (!kPaged) {
-          if (lane == 0) bulk_wait_read<0>();  // staging free again
+          if (lane == 0) bulk_wait_read<1>();  // this box's last store read
         }
         __syncwarp();
-        KVTC_TR(1)
-        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + accb * 128u;
-        const int npc = nc / 32;
-        for (int pc = 0; pc < npc; ++pc) {
-          float v[32];
-          tmem_ld32(taddr + (uint32_t)pc * 32u, v);
-          tmem_wait_ld();
-          if (pc + 1 == npc) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(acc_empty_leader + accb * 8u);
-          }
-          // 32 columns = 4 of the 8 16-byte chunks of a 64-column box row
-          const uint32_t hf = stg_row + (uint32_t)(pc >> 1) * kDecStgHalf;
-          const uint32_t c0 = (uint32_t)(pc & 1) * 4u;
+        const uint32_t srow = smem_u32(stg_w) + lane * 128;
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            sts_v4(hf + (((c0 + i) ^ sw) << 4),
-                   pack_bf16(v[8 * i], v[8 * i + 1]),
-                   pack_bf16(v[8 * i + 2], v[8 * i + 3]),
-                   pack_bf16(v[8 * i + 4], v[8 * i + 5]),
-                   pack_bf16(v[8 * i + 6], v[8 * i + 7]));
-        }
+        for (int i = 0; i < 8; ++i)
+          sts_v4(srow + (((uint32_t)i ^ sw) << 4),
+                 pack_bf16(v[8 * i], v[8 * i + 1]),
+                 pack_bf16(v[8 * i + 2], v[8 * i + 3]),
+                 pack_bf16(v[8 * i + 4], v[8 * i + 5]),
+                 pack_bf16(v[8 * i + 6], v[8 * i + 7]));
         KVTC_TR(2)
         if constexpr (!kPaged) {
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0 && wrow0 < t.tc) {
-            for (int h = 0; h < nc / 64; ++h)
-              tma_store_2d(&p.tm_out[t.seg], ch * nc + h * 64, wrow0,
-                           stg_w + h * kDecStgHalf);
+          if (lane == 0) {
+            if (wrow0 < t.tc)
+              tma_store_2d(&p.tm_out[t.seg], ch * nc + col0, wrow0, stg_w);
+            bulk_commit();
           }
-          if (lane == 0) bulk_commit();
         } else {
           __syncwarp();
-          // a row chunk (nc * 2 bytes) is written by nc / 8 lanes, 16 bytes
-          // each, so every store instruction covers whole 128-byte lines
-          const int lanes_per_row = nc / 8;
-          const int rows_per_it = 32 / lanes_per_row;
-          const int sub = lane % lanes_per_row;
-          for (int r0 = 0; r0 < 32; r0 += rows_per_it) {
-            const int r = r0 + lane / lanes_per_row;
+          // 8 lanes per 128-byte row, four rows per store instruction
+          for (int r0 = 0; r0 < 32; r0 += 4) {
+            const int r = r0 + (lane >> 3);
+            const int sub = lane & 7;
             char* rp = reinterpret_cast<char*>(__shfl_sync(
                 0xFFFFFFFFu, reinterpret_cast<uintptr_t>(rowp), r));
-            const int c16 = sub & 7;
             const uint4 val = *reinterpret_cast<const uint4*>(
-                stg_w + (sub >> 3) * kDecStgHalf + r * 128 +
-                ((c16 ^ (r & 7)) << 4));
+                stg_w + r * 128 + ((sub ^ (r & 7)) << 4));
             if (rp)
-              *reinterpret_cast<uint4*>(rp + (int64_t)ch * nc * 2 + sub * 16) =
-                  val;
+              *reinterpret_cast<uint4*>(rp + (int64_t)(ch * nc + col0) * 2 +
+                                        sub * 16) = val;
           }
+          __syncwarp();
         }
         KVTC_TR(3)
       }

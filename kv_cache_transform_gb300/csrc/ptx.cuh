@@ -160,6 +160,18 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst,
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d_pair(void* smem_dst,
+                                                 const void* tmap, int32_t x,
+                                                 int32_t y, int32_t z,
+                                                 uint32_t bar_cluster_addr) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::"
+      "bytes.cta_group::2 [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar_cluster_addr)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
