@@ -54,13 +54,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
                : "memory");
 }
 
-// arrive on an mbarrier given by its shared::cluster address (possibly in
-// the peer CTA of the pair)
+// Arrive on an mbarrier given by its shared::cluster address (possibly in
+// the peer CTA of the pair).  Default (.release.cta) semantics: every use
+// hands over TMEM, whose accesses are already complete (tcgen05.wait::ld /
+// wait::st) and ordered by the tcgen05 fences around the barrier.  The
+// .release.cluster form costs ~320 cycles per arrive and, issued by many
+// warps at once, measurably slows the MMAs running on the same SM.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile(
-      "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
-          cluster_addr)
-      : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(
+                   cluster_addr)
+               : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar,
