@@ -371,13 +371,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
           tc_fence_after();
           KVTC_TR(3)
           // K block kb of this CTA's half lies at kb * half * 128 bytes; the
-          // descriptor start address advances 32 bytes (2 units) per K=16
+          // descriptor start address advances 32 bytes (2 units) per K=16.
+          // The tensor pipe queues almost nothing ahead, so the steps are
+          // one unrolled, branch-free run of predicated MMAs whose operands
+          // are all simple offsets of two registers.
           const uint64_t bdesc = desc_b0 + (uint64_t)(s * (kDecBStage >> 4));
-          for (int step = 0; step < ksteps; ++step)
-            mma_ts_pair(d, a_col + (uint32_t)step * 8u,
-                        bdesc + (uint64_t)((step >> 2) * kb_units +
-                                           (step & 3) * 2),
-                        idesc, step > 0);
+#pragma unroll
+          for (int step = 0; step < kMaxK / kGroup + 1; ++step)
+            mma_ts_pair_if(d, a_col + (uint32_t)step * 8u,
+                           bdesc + (uint64_t)((step >> 2) * kb_units +
+                                              (step & 3) * 2),
+                           idesc, step > 0, step < ksteps);
           tc_commit_pair(&empty_b[s], 3);
           if (++s == (uint32_t)nst) {
             s = 0;
