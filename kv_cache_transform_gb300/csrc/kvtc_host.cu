@@ -120,35 +120,37 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2-D tiled map: inner dimension `cols` (contiguous), `rows` rows with a
-// stride of `row_bytes`, box {64, box_rows}, 128-byte swizzle.
-bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base,
-               uint64_t cols, uint64_t rows, uint64_t row_bytes,
-               uint32_t box_rows) {
+// K-block-major operand [nblk][rows][64] (16-bit elements): 3-D map
+// {64, rows, nblk}, box {64, box_rows, box_blk}, 128-byte swizzle; a box
+// lands in shared memory as box_blk [box_rows][64] tiles.
+bool encode_blocked_3d(CUtensorMap* m, CUtensorMapDataType dt,
+                       const void* base, uint64_t rows, uint64_t nblk,
+                       uint32_t box_rows, uint32_t box_blk) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {64u, box_rows};
-  cuuint32_t estr[2] = {1u, 1u};
-  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  cuuint64_t dims[3] = {64, rows, nblk};
+  cuuint64_t strides[2] = {128, 128ull * rows};
+  cuuint32_t box[3] = {64u, box_rows, box_blk};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// V_dec, K-block major [nkb][D][64] fp16: box {64, rows, nkb}, 128-byte
-// swizzle; the box lands in shared memory as nkb [rows][64] tiles.
-bool encode_vdec_3d(CUtensorMap* m, const void* base, uint64_t D,
-                    uint64_t nkb, uint32_t rows) {
+// Row-major bf16 rows [rows][cols] (row stride row_bytes) viewed as
+// {64 columns, rows, cols / 64 column blocks}: one box {64, 128 rows, 2}
+// brings 128 rows of two consecutive 64-column K blocks, landing in shared
+// memory as two [128][64] tiles; 128-byte swizzle.
+bool encode_rows_kblocks(CUtensorMap* m, const void* base, uint64_t cols,
+                         uint64_t rows, uint64_t row_bytes) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
-  cuuint64_t dims[3] = {64, D, nkb};
-  cuuint64_t strides[2] = {128, 128ull * D};
-  cuuint32_t box[3] = {64u, rows, (cuuint32_t)nkb};
+  cuuint64_t dims[3] = {64, rows, cols / 64};
+  cuuint64_t strides[2] = {row_bytes, 128};
+  cuuint32_t box[3] = {64u, (cuuint32_t)kTileM, 2u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base),
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -438,7 +440,7 @@ int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
         double v;
         std::memcpy(&v, V + (size_t)a * h.D + d, 8);
         const uint16_t eb = bf16_bits_rne(v);
-        venc[(size_t)a * h.D + d] = eb;
+        venc[((size_t)(d >> 6) * h.k + a) * 64 + (d & 63)] = eb;
         vd(d, a) = fp16_bits_rne(v);
         uint32_t u = (uint32_t)eb << 16;
         float ef;
@@ -470,13 +472,16 @@ int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
     s.R = h.R;
     s.nc = (h.D % 128 == 0) ? 128 : 64;
     s.kp = kp;
-    // each CTA of a pair loads half of the N rows of the B operand, all K
-    // blocks at once
-    if (!encode_vdec_3d(&s.tm_vdec, dev + o.vdec, (uint64_t)h.D,
-                        (uint64_t)((kp + 63) / 64), (uint32_t)(s.nc / 2)) ||
-        !encode_2d(&s.tm_venc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dev + o.venc,
-                   (uint64_t)h.D, (uint64_t)h.k, 2ull * h.D,
-                   (uint32_t)(h.k / 2))) {
+    // each CTA of a pair loads half of the N rows of the B operand, several K
+    // blocks at once (V_dec: every K block of a chunk half; V_enc: two K
+    // blocks of the component half)
+    if (!encode_blocked_3d(&s.tm_vdec, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                           dev + o.vdec, (uint64_t)h.D,
+                           (uint64_t)((kp + 63) / 64), (uint32_t)(s.nc / 2),
+                           (uint32_t)((kp + 63) / 64)) ||
+        !encode_blocked_3d(&s.tm_venc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                           dev + o.venc, (uint64_t)h.k, (uint64_t)(h.D / 64),
+                           (uint32_t)(h.k / 2), 2u)) {
       cudaFree(c->pool);
       delete c;
       return KVTC_ECUDA;
@@ -616,8 +621,8 @@ int kvtc_compress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
     for (size_t i = i0; i < i1; ++i) {
       const HostStream& h = c->hs[cs[i]];
       CompSeg& g = p->seg[i - i0];
-      if (!encode_2d(&g.tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, src[slot[i]],
-                     (uint64_t)h.D, (uint64_t)(s_ + tc), 2ull * ld, kTileM)) {
+      if (!encode_rows_kblocks(&g.tm_x, src[slot[i]], (uint64_t)h.D,
+                               (uint64_t)(s_ + tc), 2ull * ld)) {
         ret = KVTC_ECUDA;
         break;
       }
@@ -635,8 +640,10 @@ int kvtc_compress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
     p->nseg = (int32_t)(i1 - i0);
     p->total_tiles = tiles;
     p->tiles_per_seg = (int32_t)((tc + kPairM - 1) / kPairM);
-    p->b_bytes_max = kmax * 64;  // half of V_enc's k rows per CTA
-    p->stage_bytes = kTileM * 128 + p->b_bytes_max;
+    // a stage holds two K blocks: x [2][128][64] and this CTA's half of
+    // V_enc's k rows [2][k/2][64]
+    p->b_bytes_max = 2 * kmax * 64;
+    p->stage_bytes = 2 * kTileM * 128 + p->b_bytes_max;
     p->rec_stg_words = rmax / 4;
     int nst = 6;
     while (nst > 2 && compress_smem_bytes(nst, p->stage_bytes,

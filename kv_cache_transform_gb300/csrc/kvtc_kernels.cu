@@ -692,10 +692,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
         const DevStream* ds = p.streams + g.cs;
         const int nkb = ds->D / kAtomK;
         const int half = ds->k >> 1;
-        // both CTAs' A tiles and B halves land on the leader's barrier
+        // a stage is two K blocks; both CTAs' x tiles and V_enc halves land
+        // on the leader's barrier (a box past the last K block is filled
+        // with zeros and still counts its full bytes)
         const uint32_t bytes_pair =
-            2u * ((uint32_t)kCompAStage + (uint32_t)half * 128u);
-        for (int kb = 0; kb < nkb; ++kb) {
+            4u * ((uint32_t)kCompAStage + (uint32_t)half * 128u);
+        for (int kb = 0; kb < nkb; kb += 2) {
           KVTC_TR(0)
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) {
             ok = false;
@@ -704,11 +706,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
           KVTC_TR(1)
           uint8_t* st = smem + s * stage_bytes;
           if (leader) mbar_arrive_expect_tx(&full[s], bytes_pair);
-          tma_load_2d_pair(st, &g.tm_x, kb * kAtomK,
-                           g.row0 + tile * kPairM + (int)rank * kTileM,
+          tma_load_3d_pair(st, &g.tm_x, 0,
+                           g.row0 + tile * kPairM + (int)rank * kTileM, kb,
                            full_leader + s * 8u);
-          tma_load_2d_pair(st + kCompAStage, &ds->tm_venc, kb * kAtomK,
-                           (int)rank * half, full_leader + s * 8u);
+          tma_load_3d_pair(st + 2 * kCompAStage, &ds->tm_venc, 0,
+                           (int)rank * half, kb, full_leader + s * 8u);
           ++it_b;
           if (++s == (uint32_t)nst) {
             s = 0;
@@ -738,12 +740,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
       bool ok = true;
       const uint64_t desc_s0 = sw128_desc(smem_u32(smem));
       const uint64_t stage_units = (uint64_t)(stage_bytes >> 4);
-      const uint64_t b_units = (uint64_t)(kCompAStage >> 4);
+      const uint64_t b_units = (uint64_t)((2 * kCompAStage) >> 4);
+      const uint64_t a_kb_units = (uint64_t)(kCompAStage >> 4);
       for (int item = pair; item < total && ok; item += npairs) {
         const CompSeg& g = p.seg[find_comp_seg(p, item)];
         const DevStream* ds = p.streams + g.cs;
         const int nkb = ds->D / kAtomK;
         const uint32_t idesc = make_idesc(256, (uint32_t)ds->k, 1);
+        // one K block of this CTA's V_enc half, in 16-byte units
+        const uint64_t b_kb_units = (uint64_t)((ds->k >> 1) * 128 / 16);
         const uint32_t accb = it & 1u;
         KVTC_TR(0)
         if (!mbar_wait(&acc_empty[accb], ((it >> 1) & 1u) ^ 1u, abort_flag)) {
@@ -753,7 +758,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
         tc_fence_after();
         KVTC_TR(1)
         const uint32_t d = tmem + accb * 256u;
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = 0; kb < nkb; kb += 2) {
           KVTC_TR(0)
           if (!mbar_wait(&full[s], ph, abort_flag)) {
             ok = false;
@@ -761,12 +766,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
           }
           tc_fence_after();
           KVTC_TR(2)
+          // two K blocks, four K=16 steps each: one unrolled run (the
+          // second block predicated off past the last K block)
           const uint64_t ad = desc_s0 + s * stage_units;
           const uint64_t bd = ad + b_units;
-          mma_ss_pair(d, ad, bd, idesc, kb > 0);
-          mma_ss_pair(d, ad + 2u, bd + 2u, idesc, 1u);
-          mma_ss_pair(d, ad + 4u, bd + 4u, idesc, 1u);
-          mma_ss_pair(d, ad + 6u, bd + 6u, idesc, 1u);
+          const uint32_t two = kb + 1 < nkb;
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int st = 0; st < 4; ++st)
+              mma_ss_pair_if(d, ad + (uint64_t)j * a_kb_units + 2u * st,
+                             bd + (uint64_t)j * b_kb_units + 2u * st, idesc,
+                             (kb | j | st) != 0, j == 0 || two);
           tc_commit_pair(&empty[s], 3);
           if (++s == (uint32_t)nst) {
             s = 0;

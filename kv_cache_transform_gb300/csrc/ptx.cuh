@@ -291,6 +291,20 @@ __device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
+// mma_ss_pair issued only when `issue` is nonzero (predicated, no branch).
+__device__ __forceinline__ void mma_ss_pair_if(uint32_t d_tmem, uint64_t a_desc,
+                                               uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate,
+                                               uint32_t issue) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
+      : "memory");
+}
 // mma_ts_pair issued only when `issue` is nonzero (a predicated
 // instruction, no branch), so fixed-length unrolled MMA sequences can cover
 // a variable number of K steps without breaking the issue stream.
