@@ -643,6 +643,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
   uint64_t* acc_full = bar + 2 * kCompMaxStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* mma_done = acc_full + 4;
+  uint64_t* rec_full = acc_full + 5;  // [2 buffers][4 quadrants]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 32);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 33);
 
@@ -662,8 +663,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 8);   // 4 epilogue warps in each CTA
+      mbar_init(&acc_empty[i], 16);  // 8 epilogue warps in each CTA
     }
+    for (int i = 0; i < 8; ++i) mbar_init(&rec_full[i], 2);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -798,24 +800,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
     __syncwarp();
   } else {
     // ------------------------- epilogue: quantise + bit-plane records
-    // Two sets of four warps (one per TMEM lane quadrant each): set 0 takes
-    // the even tiles (accumulator 0), set 1 the odd ones.
+    // Two sets of four warps (one per TMEM lane quadrant each) share every
+    // tile: set 0 codes the first half of the kept groups, set 1 the rest,
+    // so an accumulator is released after half a tile's work.  The two
+    // warps of a quadrant build their 32 tokens' records in one staging
+    // buffer (two buffers alternate between tiles), meet on an mbarrier,
+    // and each writes half of the records out.
     const int q = warp & 3;
     const uint32_t set = (uint32_t)(warp - 2) >> 2;
-    uint32_t* stg = sRec + (warp - 2) * (rec_words * 33);
-    const uint32_t stg_addr = smem_u32(stg);
     const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
     uint32_t it = 0;
     bool ok = true;
     KVTC_TR_DECL
     for (int item = pair; item < total; item += npairs, ++it) {
-      const uint32_t accb = it & 1u;
-      if (accb != set) continue;
+      const uint32_t accb = it & 1u;  // accumulator and staging buffer
+      uint32_t* stg = sRec + (accb * 4u + (uint32_t)q) * (rec_words * 33);
+      const uint32_t stg_addr = smem_u32(stg);
       const int sg = find_comp_seg(p, item);
       const CompSeg& g = p.seg[sg];
       const int tile = item - sg * p.tiles_per_seg;
       const DevStream* ds = p.streams + g.cs;
       const int R = ds->R, Ga = ds->Ga;
+      // set 0: groups [0, gh), set 1: [gh, Ga); gh even (pairs of groups
+      // per TMEM load)
+      const int gh = min(Ga, ((Ga + 3) >> 2) << 1);
+      const int a_begin = set ? gh : 0, a_end = set ? Ga : gh;
       KVTC_TR(0)
       if (!mbar_wait(&acc_full[accb], (it >> 1) & 1u, abort_flag)) {
         ok = false;
@@ -825,16 +834,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
       KVTC_TR(1)
       const int row0 = tile * kPairM + (int)rank * kTileM + q * 32;
       const int nvalid = min(max(g.tc - row0, 0), 32);
-      for (int w = 0; w < (R >> 2); ++w) stg[w * 33 + lane] = 0u;
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + accb * 256u;
+      if ((set == 1) == (Ga > gh)) {
+        // the warp coding the last group zeroes the record's padding:
+        // fields and planes cover bytes [0, used) exactly
+        const int used = Ga ? ds->poff[Ga - 1] + 2 * ds->bits[Ga - 1] : 0;
+        if (used & 2)
+          sts_u16(stg_addr + (uint32_t)(((used >> 2) * 33 + lane) * 4 + 2),
+                  0u);
+        for (int w = (used + 3) >> 2; w < (R >> 2); ++w) stg[w * 33 + lane] = 0u;
+      }
+      if (a_begin >= a_end) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty_leader + accb * 8u);
+      }
       bool range_err = false;
-      for (int a0 = 0; a0 < Ga; a0 += 2) {
+      for (int a0 = a_begin; a0 < a_end; a0 += 2) {
         // two groups per TMEM round trip (the second may lie past k when Ga
         // is odd; it is inside the allocation and left unused)
         float v2[32];
         tmem_ld32(taddr + (uint32_t)a0 * 16u, v2);
         tmem_wait_ld();
-        if (a0 + 2 >= Ga) {
+        if (a0 + 2 >= a_end) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(acc_empty_leader + accb * 8u);
@@ -842,7 +864,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int a = a0 + h;
-          if (a >= Ga) break;
+          if (a >= a_end) break;
           float* v = v2 + 16 * h;
           const float4* m4 = reinterpret_cast<const float4*>(ds->m + a * 16);
 #pragma unroll
@@ -902,8 +924,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
       if (range_err && lane < nvalid) atomicOr(p.status, KVTC_FLAG_RANGE);
       __syncwarp();
       KVTC_TR(2)
+      // both warps of the quadrant have staged their groups
+      if (lane == 0) mbar_arrive(&rec_full[accb * 4u + (uint32_t)q]);
+      if (!mbar_wait(&rec_full[accb * 4u + (uint32_t)q], (it >> 1) & 1u,
+                     abort_flag)) {
+        ok = false;
+        break;
+      }
+      // set h writes tokens [16 h, 16 h + 16) of the quadrant
       uint8_t* rbase = g.rec + (int64_t)row0 * R;
-      for (int o = lane * 16; o < 32 * R; o += 512) {
+      const int o_end = (int)(set + 1) * 16 * R;
+      for (int o = (int)set * 16 * R + lane * 16; o < o_end; o += 512) {
         const int tr = o / R;
         const int wd = (o - tr * R) >> 2;
         if (tr < nvalid)
