@@ -128,19 +128,18 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 // ======================================================================
 //                               decompress
 // ======================================================================
-constexpr int kDecWarps = 18;  // 0 TMA, 1 MMA, 2-9 prologue, 10-17 epilogue
+constexpr int kDecWarps = 26;  // 0 TMA, 1 MMA, 2-9 prologue, 10-25 epilogue
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kDecNC = 128;
 constexpr int kDecMaxStages = 8;
 // one B stage = this CTA's half of a chunk, every K block: [kb][64 rows][64]
 constexpr int kDecBStage = (kDecNC / 2) * 128 * (kMaxK / 64 + 1);
-constexpr int kDecStgHalf = 32 * 128;             // 32 rows x 64 bf16, SW128
-constexpr int kDecStgWarp = 2 * kDecStgHalf;       // one 128-column chunk
+constexpr int kDecStgWarp = 32 * 128;  // 32 rows x 64 bf16, SW128
 constexpr int kDecBarBytes = 512;
-// Shared memory: [B ring: nstages x 8 KB][staging: 8 warps x 8 KB]
+// Shared memory: [B ring: nstages x 32 KB][staging: 16 warps x 4 KB]
 // [records: 8 warps x rec_words x 33 u32][barriers][misc]
 int decompress_smem_bytes(int nstages, int rec_words) {
-  return nstages * kDecBStage + 8 * kDecStgWarp + 8 * rec_words * 33 * 4 +
+  return nstages * kDecBStage + 16 * kDecStgWarp + 8 * rec_words * 33 * 4 +
          kDecBarBytes + 64 + 1024;
 }
 int decompress_stages(int rec_words) {
@@ -234,7 +233,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
   const int rec_words = p.rec_words;
   uint8_t* sB = smem;
   uint8_t* sStg = smem + nst * kDecBStage;
-  uint32_t* sRec = reinterpret_cast<uint32_t*>(sStg + 8 * kDecStgWarp);
+  uint32_t* sRec = reinterpret_cast<uint32_t*>(sStg + 16 * kDecStgWarp);
   uint64_t* bar = reinterpret_cast<uint64_t*>(
       reinterpret_cast<uint8_t*>(sRec) + 8 * rec_words * 33 * 4);
   uint64_t* full_b = bar;                       // [nst], leader's used
@@ -505,16 +504,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
     if (!ok && lane == 0) raise_abort(abort_flag, p.status);
   } else {
     // -------------- epilogue: bf16 rows (the mean came in the MMA)
-    // Two sets of four warps (one per TMEM lane quadrant each) share every
-    // chunk: set h takes its columns [64 h, 64 h + 64), so an accumulator
-    // is released after one TMEM round trip.  A warp stages its 32 rows x
-    // 64 columns as one 128-byte-swizzled box (two boxes alternate between
-    // chunks) and writes it with a TMA tensor store (contiguous output) or
-    // with coalesced 16-byte stores through the block table (paged).
+    // Two groups of eight warps take alternate chunks (group g the chunks
+    // in accumulator g); within a group two sets of four warps (one per
+    // TMEM lane quadrant each) split the columns: set h takes [64 h,
+    // 64 h + 64), so an accumulator is released after one TMEM round trip
+    // and each warp has two chunk times for its work.  A warp stages its
+    // 32 rows x 64 columns as one 128-byte-swizzled box and writes it with
+    // a TMA tensor store (contiguous output) or with coalesced 16-byte
+    // stores through the block table (paged).
     constexpr bool kPaged = std::is_same<P, PagedParams>::value;
+    const int e = warp - 10;
+    const uint32_t grp = (uint32_t)e >> 3;
     const int q = warp & 3;
-    const int col0 = ((warp - 10) >> 2) * 64;
-    uint8_t* stg_base = sStg + (warp - 10) * kDecStgWarp;
+    const int col0 = ((e >> 2) & 1) * 64;
+    uint8_t* stg_w = sStg + e * kDecStgWarp;
     const uint32_t sw = (uint32_t)(lane & 7);
     const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
     uint32_t chunk = 0;
@@ -533,6 +536,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       }
       for (int ch = 0; ch < nch; ++ch, ++chunk) {
         const uint32_t accb = chunk & 1u;
+        if (accb != grp) continue;
         KVTC_TR(0)
         if (!mbar_wait(&acc_full[accb], (chunk >> 1) & 1u, abort_flag)) {
           ok = false;
@@ -540,31 +544,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         }
         tc_fence_after();
         KVTC_TR(1)
-        float v[64];
+        // 64 columns as 32 bf16 pairs, packed 32 columns at a time
+        uint32_t pk[32];
         if (mine) {
           const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) +
                                  accb * 128u + (uint32_t)col0;
-          tmem_ld32(taddr, v);
-          tmem_ld32(taddr + 32u, v + 32);
-          tmem_wait_ld();
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            float v[32];
+            tmem_ld32(taddr + (uint32_t)hh * 32u, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[16 * hh + i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+          }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(acc_empty_leader + accb * 8u);
         if (!mine) continue;
-        uint8_t* stg_w = stg_base + (chunk & 1u) * kDecStgHalf;
         if constexpr (!kPaged) {
-          if (lane == 0) bulk_wait_read<1>();  // this box's last store read
+          if (lane == 0) bulk_wait_read<0>();  // the last store read stg_w
         }
         __syncwarp();
         const uint32_t srow = smem_u32(stg_w) + lane * 128;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          sts_v4(srow + (((uint32_t)i ^ sw) << 4),
-                 pack_bf16(v[8 * i], v[8 * i + 1]),
-                 pack_bf16(v[8 * i + 2], v[8 * i + 3]),
-                 pack_bf16(v[8 * i + 4], v[8 * i + 5]),
-                 pack_bf16(v[8 * i + 6], v[8 * i + 7]));
+          sts_v4(srow + (((uint32_t)i ^ sw) << 4), pk[4 * i], pk[4 * i + 1],
+                 pk[4 * i + 2], pk[4 * i + 3]);
         KVTC_TR(2)
         if constexpr (!kPaged) {
           fence_proxy_async_smem();
