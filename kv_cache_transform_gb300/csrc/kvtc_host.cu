@@ -470,7 +470,7 @@ int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
     s.k = h.k;
     s.Ga = h.Ga;
     s.R = h.R;
-    s.nc = (h.D % 128 == 0) ? 128 : 64;
+    s.nc = (h.D % 256 == 0) ? 256 : (h.D % 128 == 0) ? 128 : 64;
     s.kp = kp;
     // each CTA of a pair loads half of the N rows of the B operand, several K
     // blocks at once (V_dec: every K block of a chunk half; V_enc: two K

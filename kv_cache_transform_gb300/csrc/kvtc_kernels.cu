@@ -130,10 +130,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 // ======================================================================
 constexpr int kDecWarps = 26;  // 0 TMA, 1 MMA, 2-9 prologue, 10-25 epilogue
 constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kDecNC = 128;
+constexpr int kDecMaxNC = 256;  // widest output chunk (one MMA's N)
 constexpr int kDecMaxStages = 8;
 // one B stage = this CTA's half of a chunk, every K block: [kb][64 rows][64]
-constexpr int kDecBStage = (kDecNC / 2) * 128 * (kMaxK / 64 + 1);
+constexpr int kDecBStage = (kDecMaxNC / 2) * 128 * (kMaxK / 64 + 1);
 constexpr int kDecStgWarp = 32 * 128;  // 32 rows x 64 bf16, SW128
 constexpr int kDecBarBytes = 512;
 // Shared memory: [B ring: nstages x 32 KB][staging: 16 warps x 4 KB]
@@ -147,7 +147,8 @@ int decompress_stages(int rec_words) {
   while (n > 2 && decompress_smem_bytes(n, rec_words) > 232448) --n;
   return n;
 }
-// TMEM columns: accumulators at 0 and 128, A operands at 256 and 384.
+// TMEM columns: accumulators in [0, 256) (256 / nc of them, nc columns
+// each), A operands at 256 and 384.
 constexpr uint32_t kDecTmemCols = 512;
 
 
@@ -240,9 +241,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
   uint64_t* empty_b = bar + kDecMaxStages;      // [nst]
   uint64_t* a_full = bar + 2 * kDecMaxStages;   // [2], leader's used
   uint64_t* a_empty = a_full + 2;               // [2]
-  uint64_t* acc_full = a_full + 4;              // [2]
-  uint64_t* acc_empty = a_full + 6;             // [2], leader's used
-  uint64_t* mma_done = a_full + 8;
+  uint64_t* acc_full = a_full + 4;              // [4]
+  uint64_t* acc_empty = a_full + 8;             // [4], leader's used
+  uint64_t* mma_done = a_full + 12;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(
       reinterpret_cast<uint8_t*>(bar) + kDecBarBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -264,8 +265,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&a_full[i], 8);      // 4 prologue warps in each CTA
       mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < 4; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 16);  // 8 epilogue warps in each CTA
+      // the epilogue warps of both CTAs that read a chunk arrive with
+      // counts adding up to 32 whatever the chunk width
+      mbar_init(&acc_empty[i], 32);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -334,11 +339,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       KVTC_TR_DECL
       uint32_t chunk = 0, it = 0, s = 0, ph = 0;
       bool ok = true;
+      // the next chunk's accumulator and B stage, when already known ready
+      bool acc_ready = false, b_ready = false;
       const uint64_t desc_b0 = sw128_desc(smem_u32(sB));
       for (int item = pair; item < total && ok; item += npairs) {
         const DecTile t = resolve(p, item);
         const DevStream* ds = p.streams + t.cs;
         const int nc = ds->nc, nch = ds->D / nc;
+        // 256 / nc accumulators of nc columns: log2 of their count
+        const uint32_t lg = nc == 256 ? 0u : nc == 128 ? 1u : 2u;
+        const uint32_t nbm = (1u << lg) - 1u;
         const int ksteps = ds->kp / kGroup;  // kept groups + the mean step
         const int kb_units = (ds->nc / 2) * 128 / 16;  // one K block, >> 4
         const uint32_t idesc = make_idesc(256, (uint32_t)nc, 0);
@@ -352,18 +362,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         KVTC_TR(1)
         const uint32_t a_col = tmem + 256u + abuf * 128u;
         for (int ch = 0; ch < nch && ok; ++ch) {
-          const uint32_t accb = chunk & 1u;
+          const uint32_t accb = chunk & nbm;
           KVTC_TR(0)
-          if (!mbar_wait(&acc_empty[accb], ((chunk >> 1) & 1u) ^ 1u,
+          if (!acc_ready &&
+              !mbar_wait(&acc_empty[accb], ((chunk >> lg) & 1u) ^ 1u,
                          abort_flag)) {
             ok = false;
             break;
           }
-          tc_fence_after();
           KVTC_TR(2)
-          const uint32_t d = tmem + accb * 128u;
+          const uint32_t d = tmem + accb * (uint32_t)nc;
           KVTC_TR(0)
-          if (!mbar_wait(&full_b[s], ph, abort_flag)) {
+          if (!b_ready && !mbar_wait(&full_b[s], ph, abort_flag)) {
             ok = false;
             break;
           }
@@ -375,12 +385,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
           // one unrolled, branch-free run of predicated MMAs whose operands
           // are all simple offsets of two registers.
           const uint64_t bdesc = desc_b0 + (uint64_t)(s * (kDecBStage >> 4));
+          // the next chunk's barriers are tested (never waited on) right
+          // after the first MMA, so the test overlaps the MMA run
+          const uint32_t s_next = s + 1 == (uint32_t)nst ? 0u : s + 1;
+          const uint32_t ph_next = s + 1 == (uint32_t)nst ? ph ^ 1u : ph;
+          const uint32_t c_next = chunk + 1;
 #pragma unroll
-          for (int step = 0; step < kMaxK / kGroup + 1; ++step)
+          for (int step = 0; step < kMaxK / kGroup + 1; ++step) {
             mma_ts_pair_if(d, a_col + (uint32_t)step * 8u,
                            bdesc + (uint64_t)((step >> 2) * kb_units +
                                               (step & 3) * 2),
                            idesc, step > 0, step < ksteps);
+            if (step == 0) {
+              acc_ready = mbar_test_wait(&acc_empty[c_next & nbm],
+                                         ((c_next >> lg) & 1u) ^ 1u);
+              b_ready = mbar_test_wait(&full_b[s_next], ph_next);
+            }
+          }
           tc_commit_pair(&empty_b[s], 3);
           if (++s == (uint32_t)nst) {
             s = 0;
@@ -504,19 +525,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
     if (!ok && lane == 0) raise_abort(abort_flag, p.status);
   } else {
     // -------------- epilogue: bf16 rows (the mean came in the MMA)
-    // Two groups of eight warps take alternate chunks (group g the chunks
-    // in accumulator g); within a group two sets of four warps (one per
-    // TMEM lane quadrant each) split the columns: set h takes [64 h,
-    // 64 h + 64), so an accumulator is released after one TMEM round trip
-    // and each warp has two chunk times for its work.  A warp stages its
-    // 32 rows x 64 columns as one 128-byte-swizzled box and writes it with
-    // a TMA tensor store (contiguous output) or with coalesced 16-byte
+    // Sixteen warps.  With 256 / nc accumulators, 16 nc / 256 warps read
+    // each chunk (group g takes the chunks in accumulator g); within a
+    // group, sets of four warps (one per TMEM lane quadrant each) split the
+    // chunk's columns 64 apiece, so an accumulator is released after one
+    // TMEM round trip of every warp of its group.  A warp stages its 32
+    // rows x 64 columns as one 128-byte-swizzled box and writes it with a
+    // TMA tensor store (contiguous output) or with coalesced 16-byte
     // stores through the block table (paged).
     constexpr bool kPaged = std::is_same<P, PagedParams>::value;
     const int e = warp - 10;
-    const uint32_t grp = (uint32_t)e >> 3;
     const int q = warp & 3;
-    const int col0 = ((e >> 2) & 1) * 64;
     uint8_t* stg_w = sStg + e * kDecStgWarp;
     const uint32_t sw = (uint32_t)(lane & 7);
     const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
@@ -527,18 +546,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       const DecTile t = resolve(p, item);
       const DevStream* ds = p.streams + t.cs;
       const int D = ds->D, nc = ds->nc, nch = D / nc;
-      const bool mine = col0 < nc;
+      const uint32_t lg = nc == 256 ? 0u : nc == 128 ? 1u : 2u;
+      const uint32_t nbm = (1u << lg) - 1u;
+      // warps per chunk 16 >> lg; this warp's group and 64-column set
+      const uint32_t grp = (uint32_t)e >> (4 - lg);
+      const int col0 = ((e & ((16 >> lg) - 1)) >> 2) * 64;
       const int wrow0 = t.tile * kPairM + (int)rank * kTileM + q * 32;
       const int row = wrow0 + lane;
       char* rowp = nullptr;
       if constexpr (kPaged) {
-        if (mine && row < t.tc) rowp = dec_row_ptr(p, t, row, D);
+        if (row < t.tc) rowp = dec_row_ptr(p, t, row, D);
       }
       for (int ch = 0; ch < nch; ++ch, ++chunk) {
-        const uint32_t accb = chunk & 1u;
+        const uint32_t accb = chunk & nbm;
         if (accb != grp) continue;
         KVTC_TR(0)
-        if (!mbar_wait(&acc_full[accb], (chunk >> 1) & 1u, abort_flag)) {
+        if (!mbar_wait(&acc_full[accb], (chunk >> lg) & 1u, abort_flag)) {
           ok = false;
           break;
         }
@@ -546,9 +569,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         KVTC_TR(1)
         // 64 columns as 32 bf16 pairs, packed 32 columns at a time
         uint32_t pk[32];
-        if (mine) {
+        {
           const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) +
-                                 accb * 128u + (uint32_t)col0;
+                                 accb * (uint32_t)nc + (uint32_t)col0;
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             float v[32];
@@ -561,8 +584,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(acc_empty_leader + accb * 8u);
-        if (!mine) continue;
+        if (lane == 0)
+          mbar_arrive_cluster_n(acc_empty_leader + accb * 8u, 1u << lg);
         if constexpr (!kPaged) {
           if (lane == 0) bulk_wait_read<0>();  // the last store read stg_w
         }
