@@ -94,7 +94,9 @@ typedef struct kvtc_calib kvtc_calib;
  *                      with kvtc_calib_free).
  * Derived on load: bf16 V_kept (projection), fp16 V_kept (reconstruction),
  * fp32 mu and fp32 m = bf16(V_kept) mu, group layout tables, TMA
- * descriptors.  Requirements: D % 64 == 0, D <= 8192, k <= 256.
+ * descriptors.  Requirements: D % 64 == 0, D <= 8192, k <= 240 (the
+ * reconstruction contracts k plus one mean step of 16 over at most 256
+ * columns), record bytes <= 256; otherwise ENOTSUP.
  * Errors: EINVAL, EFORMAT, ENOMEM, ECUDA, ENOTSUP.
  */
 int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,

@@ -108,3 +108,16 @@ def test_python_binding_raises_on_error(kv):
     with pytest.raises(kv.KvtcError) as e:
         kv.kvtc_calib_load(b"not a blob at all, definitely not" * 2)
     assert e.value.code == kv.KVTC_EFORMAT
+
+
+def test_kept_components_beyond_the_kernel_limit_are_refused(kv):
+    """k = 256 kept components (every group of a D = 256 stream at width 1)
+    is a valid blob, but the reconstruction contracts k plus one mean step
+    over at most 256 columns, so the library refuses it (ENOTSUP) while
+    parsing, before any CUDA call."""
+    D = 256
+    widths = np.ones(D // 16, dtype=np.uint8)
+    blob = calibrate.write_blob(
+        [(0, 0, np.zeros(D), np.eye(D), np.ones(D), widths)], 4, 16,
+        int(widths.size * calibrate.width_cost_units(1) * 16))
+    assert load_raw(kv, blob) == kv.KVTC_ENOTSUP
