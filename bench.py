@@ -36,9 +36,10 @@ WORKLOAD = "llama31_8b_8k"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
                   "bf16_tflops_sustained": 1700.0}
 # DRAM bytes per launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum)
-# of the kernel as it is now, per launch of the bench workload; None when the
-# kernel has changed since the capture.
-NCU_TRAFFIC = {"decompress": None, "compress": None}
+# of the kernel as it is now, per launch of the bench workload (a one-pass
+# capture of the full workload: profiles/launches_llama31_8b_8k.md); None
+# when the kernel has changed since the capture.
+NCU_TRAFFIC = {"decompress": 1091402496, "compress": 1145157632}
 
 
 def load_peaks():
