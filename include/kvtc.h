@@ -203,6 +203,21 @@ int kvtc_device_status(const kvtc_calib* calib, void* cuda_stream,
                        unsigned* flags);
 
 /*
+ * kvtc_wait_selftest -- exercise the bounded wait that every kernel of this
+ * library uses on its mbarriers (the pages have no counterpart: this is a
+ * failure-detection check).  One thread waits, for at most limit_us
+ * microseconds, on a barrier that nothing ever arrives at; when the limit
+ * runs out it sets KVTC_FLAG_TIMEOUT in the handle's sticky flag word, the
+ * same way a kernel reports a wait that ran out, and returns.  Read the
+ * flag with kvtc_device_status; the context stays usable.
+ *   limit_us    : 1 .. 2000000.
+ *   cuda_stream : the launch is enqueued on it.
+ * Errors: EINVAL, ECUDA.
+ */
+int kvtc_wait_selftest(const kvtc_calib* calib, uint32_t limit_us,
+                       void* cuda_stream);
+
+/*
  * kvtc_calib_mean_static -- the per-channel mean of calibration rows (the
  * mean that kvtc_calibrate stores for a stream), computed without
  * allocating any device memory.  The paper has no counterpart: this entry

@@ -82,6 +82,7 @@ def lib() -> ctypes.CDLL:
         "kvtc_launch_count": (ctypes.c_uint64, []),
         "kvtc_calib_mean_static": (c_i, [c_i, c_vp, c_i64, c_i64, c_i, c_vp,
                                          c_vp]),
+        "kvtc_wait_selftest": (c_i, [c_vp, ctypes.c_uint32, c_vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -248,6 +249,12 @@ def kvtc_decompress_paged(calib: Calib, layer0: int, nlayers: int,
         calib.handle, layer0, nlayers, kv_mask, _ptr_array(src), Ts, len(T),
         _ptr(block_table) or None, max_blocks, block_size, _ptr_array(cache),
         num_blocks, _stream(stream) or None), "kvtc_decompress_paged")
+
+
+def kvtc_wait_selftest(calib: Calib, limit_us: int, stream=None) -> None:
+    _check(lib().kvtc_wait_selftest(calib.handle, limit_us,
+                                    _stream(stream) or None),
+           "kvtc_wait_selftest")
 
 
 def kvtc_device_status(calib: Calib, stream=None) -> int:

@@ -880,6 +880,18 @@ int kvtc_decompress_paged(const kvtc_calib* c, int layer0, int nlayers,
   return ret;
 }
 
+int kvtc_wait_selftest(const kvtc_calib* c, uint32_t limit_us,
+                       void* cuda_stream) {
+  if (!c || limit_us < 1 || limit_us > 2000000u) return KVTC_EINVAL;
+  DeviceGuard guard(c->device);
+  if (!guard.ok) return KVTC_ECUDA;
+  return launch_wait_selftest(c->d_status, 1000ull * limit_us,
+                              static_cast<cudaStream_t>(cuda_stream)) ==
+                 cudaSuccess
+             ? KVTC_OK
+             : KVTC_ECUDA;
+}
+
 int kvtc_device_status(const kvtc_calib* c, void* cuda_stream,
                        unsigned* flags) {
   if (!c || !flags) return KVTC_EINVAL;

@@ -130,6 +130,8 @@ cudaError_t launch_decompress_paged(const PagedParams& p, int pairs,
 int max_pairs_compress(int smem_bytes);
 int max_pairs_decompress(int smem_bytes);
 cudaError_t launch_raw_copy(const RawParams& p, cudaStream_t st);
+cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns,
+                                 cudaStream_t st);
 cudaError_t launch_paged_raw(const PagedParams& p, cudaStream_t st);
 // Kernel launches issued by this library (all devices, all threads).
 void count_launch();

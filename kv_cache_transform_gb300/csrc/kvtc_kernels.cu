@@ -993,6 +993,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
 // ======================================================================
 //                                raw rows
 // ======================================================================
+// Self-test of the bounded wait every kernel above relies on: one thread
+// waits on an mbarrier that nothing will ever arrive at, with a short limit;
+// when the limit runs out it raises the same sticky flag the kernels raise
+// and returns, leaving the context usable.
+__global__ void __launch_bounds__(32) wait_selftest_kernel(unsigned* status,
+                                                           uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0 &&
+      !mbar_wait_for(&bar, 0u, &abort_flag, limit_ns))
+    atomicOr(status, KVTC_FLAG_TIMEOUT);
+}
+
 __global__ void __launch_bounds__(256) raw_copy_kernel(
     const __grid_constant__ RawParams p) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -1133,6 +1152,13 @@ cudaError_t launch_decompress(const DecParams& p, int pairs, cudaStream_t st) {
 cudaError_t launch_decompress_paged(const PagedParams& p, int pairs,
                                     cudaStream_t st) {
   return launch_dec(p, pairs, st);
+}
+
+cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns,
+                                 cudaStream_t st) {
+  count_launch();
+  wait_selftest_kernel<<<1, 32, 0, st>>>(status, limit_ns);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_raw_copy(const RawParams& p, cudaStream_t st) {

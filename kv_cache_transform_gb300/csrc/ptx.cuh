@@ -139,15 +139,21 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // a lost arrival cannot hang the GPU.
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          const volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity,
+                                              const volatile int* abort_flag,
+                                              uint64_t limit_ns) {
   if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          const volatile int* abort_flag) {
+  return mbar_wait_for(bar, parity, abort_flag, kWaitNs);
 }
 
 // Same bound without the abort flag: used to let copies and MMAs that were
