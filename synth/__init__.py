@@ -76,6 +76,19 @@ WORKLOADS = {
     "tiny": Workload("tiny", layers=1, kv=(K_STREAM,), heads=2, head_dim=64,
                      tokens=256, requests=1, rank=32, spectrum_p=1.0,
                      outliers=False, sink=4, window=16, avg_bits=2.0),
+    # edge shapes for the kernels' chunking: D an odd multiple of 64 (64-
+    # column output chunks, an odd number of 64-wide K blocks) and an odd
+    # multiple of 128 (128-column chunks)
+    "edge_d192": Workload("edge_d192", layers=1, kv=(0, 1), heads=3,
+                          head_dim=64, tokens=700, requests=1, rank=32,
+                          spectrum_p=1.0, outliers=True, sink=4, window=16,
+                          avg_bits=2.0),
+    # flat spectrum and 2.5 bits: the DP keeps 15 groups (k = 240, the
+    # widest the kernels take)
+    "edge_d384": Workload("edge_d384", layers=2, kv=(0, 1), heads=3,
+                          head_dim=128, tokens=900, requests=1, rank=384,
+                          spectrum_p=0.0, outliers=False, sink=4, window=128,
+                          avg_bits=2.5),
     "llama31_8b_8k": Workload("llama31_8b_8k", layers=32, kv=(0, 1), heads=8,
                               head_dim=128, tokens=8192, requests=1, rank=128,
                               spectrum_p=1.0, outliers=True, sink=4,

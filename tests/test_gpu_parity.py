@@ -121,6 +121,20 @@ def test_tiny_row_stride(kv, torch):
     run_roundtrip(kv, torch, "tiny", [(0, 0)], 700, ld_pad=24)
 
 
+def test_d192_64_column_chunks_odd_k_blocks(kv, torch):
+    """D = 192: 64-column output chunks (four accumulators in the ring) and
+    three 64-wide K blocks for the projection (the last stage half
+    empty)."""
+    run_roundtrip(kv, torch, "edge_d192", [(0, 0), (0, 1)], 700)
+
+
+def test_d384_128_column_chunks(kv, torch):
+    """D = 384: three 128-column output chunks (two accumulators), k = 240
+    (sixteen MMA K steps with the mean step, every predicated step on)."""
+    run_roundtrip(kv, torch, "edge_d384", [(0, 0), (0, 1), (1, 0), (1, 1)],
+                  900, ld_pad=64)
+
+
 def test_llama_shape_several_streams_ragged(kv, torch):
     stats, dstats = run_roundtrip(
         kv, torch, "llama31_8b_8k", [(3, 0), (3, 1), (4, 0), (4, 1)], 1000)
