@@ -644,7 +644,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
 // ======================================================================
 //                                compress
 // ======================================================================
-constexpr int kCompWarps = 10;  // 0 TMA, 1 MMA, 2-9 epilogue (two sets)
+constexpr int kCompWarps = 18;  // 0 TMA, 1 MMA, 2-17 epilogue (four sets)
 constexpr int kCompThreads = kCompWarps * 32;
 constexpr int kCompMaxStages = 6;
 constexpr int kCompAStage = kTileM * 128;          // [128 rows][64 bf16]
@@ -693,9 +693,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 16);  // 8 epilogue warps in each CTA
+      mbar_init(&acc_empty[i], 32);  // 16 epilogue warps in each CTA
     }
-    for (int i = 0; i < 8; ++i) mbar_init(&rec_full[i], 2);
+    for (int i = 0; i < 8; ++i) mbar_init(&rec_full[i], 4);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -830,12 +830,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
     __syncwarp();
   } else {
     // ------------------------- epilogue: quantise + bit-plane records
-    // Two sets of four warps (one per TMEM lane quadrant each) share every
-    // tile: set 0 codes the first half of the kept groups, set 1 the rest,
-    // so an accumulator is released after half a tile's work.  The two
-    // warps of a quadrant build their 32 tokens' records in one staging
-    // buffer (two buffers alternate between tiles), meet on an mbarrier,
-    // and each writes half of the records out.
+    // Four sets of four warps (one per TMEM lane quadrant each) share every
+    // tile: set s codes the s-th quarter of the kept groups (in pairs), so
+    // an accumulator is released after a quarter of a tile's work and four
+    // warps per scheduler hide each other's latency.  The four warps of a
+    // quadrant build their 32 tokens' records in one staging buffer (two
+    // buffers alternate between tiles), meet on an mbarrier, and each
+    // writes a quarter of the records out.
     const int q = warp & 3;
     const uint32_t set = (uint32_t)(warp - 2) >> 2;
     const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
@@ -851,10 +852,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
       const int tile = item - sg * p.tiles_per_seg;
       const DevStream* ds = p.streams + g.cs;
       const int R = ds->R, Ga = ds->Ga;
-      // set 0: groups [0, gh), set 1: [gh, Ga); gh even (pairs of groups
-      // per TMEM load)
-      const int gh = min(Ga, ((Ga + 3) >> 2) << 1);
-      const int a_begin = set ? gh : 0, a_end = set ? Ga : gh;
+      // set s: groups [s gq, s gq + gq) within [0, Ga); gq even (pairs of
+      // groups per TMEM load)
+      const int gq = ((Ga + 7) >> 3) << 1;
+      const int a_begin = min(Ga, (int)set * gq);
+      const int a_end = min(Ga, (int)set * gq + gq);
       KVTC_TR(0)
       if (!mbar_wait(&acc_full[accb], (it >> 1) & 1u, abort_flag)) {
         ok = false;
@@ -865,7 +867,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
       const int row0 = tile * kPairM + (int)rank * kTileM + q * 32;
       const int nvalid = min(max(g.tc - row0, 0), 32);
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + accb * 256u;
-      if ((set == 1) == (Ga > gh)) {
+      if ((int)set == (Ga ? (Ga - 1) / gq : 0)) {
         // the warp coding the last group zeroes the record's padding:
         // fields and planes cover bytes [0, used) exactly
         const int used = Ga ? ds->poff[Ga - 1] + 2 * ds->bits[Ga - 1] : 0;
@@ -961,10 +963,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
         ok = false;
         break;
       }
-      // set h writes tokens [16 h, 16 h + 16) of the quadrant
+      // set s writes tokens [8 s, 8 s + 8) of the quadrant
       uint8_t* rbase = g.rec + (int64_t)row0 * R;
-      const int o_end = (int)(set + 1) * 16 * R;
-      for (int o = (int)set * 16 * R + lane * 16; o < o_end; o += 512) {
+      const int o_end = (int)(set + 1) * 8 * R;
+      for (int o = (int)set * 8 * R + lane * 16; o < o_end; o += 512) {
         const int tr = o / R;
         const int wd = (o - tr * R) >> 2;
         if (tr < nvalid)
