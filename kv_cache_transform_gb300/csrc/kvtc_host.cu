@@ -248,6 +248,24 @@ int select_streams(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
 }
 
 // CTA pairs for `items` super-tiles, at most what can be resident at once.
+// Append a row segment to the raw-row list a tensor-core kernel copies
+// while it runs (src null: zeros).  False when the list is full.
+bool raw_list_add(RawList& r, const char* s, char* d, int64_t sld,
+                  int64_t dld, int64_t rows, int64_t row_bytes) {
+  if (rows <= 0 || row_bytes <= 0) return true;
+  if (r.nseg == kRawListMax) return false;
+  RawListSeg& g = r.seg[r.nseg++];
+  g.src = s;
+  g.dst = d;
+  g.src_ld = sld;
+  g.dst_ld = dld;
+  g.rows = (int32_t)rows;
+  g.row_bytes = (int32_t)row_bytes;
+  g.chunk_begin = r.total_chunks;
+  r.total_chunks += rows * (row_bytes / 16);
+  return true;
+}
+
 int pairs_for(int max_pairs, int items) {
   return std::max(1, std::min(items, max_pairs));
 }
@@ -557,8 +575,10 @@ int kvtc_compress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
   char* out = static_cast<char*>(dst);
 
-  // Raw sink/window rows and zero padding.
-  {
+  // With no coded tokens the raw sink/window rows and the zero padding go
+  // by a copy kernel; otherwise the compress kernel copies them while it
+  // runs (below).
+  if (tc == 0) {
     RawParams rp;
     std::memset(&rp, 0, sizeof(rp));
     auto flush = [&]() -> int {
@@ -606,11 +626,11 @@ int kvtc_compress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
               cudaSuccess)
         return KVTC_ECUDA;
     }
+    return KVTC_OK;
   }
-  if (tc == 0) return KVTC_OK;
 
   // Tensor-core projection + quantise/pack, up to kCompMaxSeg streams per
-  // launch.
+  // launch, with those streams' raw rows and padding.
   CompParams* p = new (std::nothrow) CompParams;
   if (!p) return KVTC_ENOMEM;
   int ret = KVTC_OK;
@@ -630,6 +650,18 @@ int kvtc_compress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
       g.tc = (int32_t)tc;
       g.row0 = (int32_t)s_;
       g.cs = cs[i];
+      const char* x = static_cast<const char*>(src[slot[i]]);
+      char* so = out + off[i];
+      const int64_t rb = 2LL * h.D;
+      const int64_t used = (s_ + w_) * rb + tc * h.R;
+      const int64_t pad = stream_bytes_of(c, h, T) - used;
+      if (!raw_list_add(p->raw, x, so, 2 * ld, rb, s_, rb) ||
+          !raw_list_add(p->raw, x + (T - w_) * 2 * ld, so + s_ * rb, 2 * ld,
+                        rb, w_, rb) ||
+          !raw_list_add(p->raw, nullptr, so + used, 0, pad, 1, pad)) {
+        ret = KVTC_EINVAL;
+        break;
+      }
       tiles += (int)((tc + kPairM - 1) / kPairM);
       kmax = std::max(kmax, h.k);
       rmax = std::max(rmax, h.R);
@@ -716,8 +748,10 @@ int kvtc_decompress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
   int ret = KVTC_OK;
   for (size_t gi = 0; gi < groups.size() && ret == KVTC_OK; ++gi) {
     const size_t i0 = groups[gi].first, i1 = groups[gi].second;
-    // raw rows back to their places
+    // raw rows back to their places: by the decompress kernel while it
+    // runs, or by a copy kernel when there are no coded tokens
     std::memset(rp, 0, sizeof(*rp));
+    std::memset(p, 0, sizeof(*p));
     for (size_t i = i0; i < i1; ++i) {
       const HostStream& h = c->hs[cs[i]];
       const int64_t rb = 2LL * h.D;
@@ -728,6 +762,11 @@ int kvtc_decompress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
       char* d2[2] = {x, x + (T - w_) * 2 * ld};
       for (int k2 = 0; k2 < 2; ++k2) {
         if (rows[k2] <= 0) continue;
+        if (tc > 0) {
+          if (!raw_list_add(p->raw, s2[k2], d2[k2], rb, 2 * ld, rows[k2], rb))
+            ret = KVTC_EINVAL;
+          continue;
+        }
         if (rp->nseg == kRawMaxSeg) {
           if (launch_raw_copy(*rp, stream) != cudaSuccess) ret = KVTC_ECUDA;
           rp->nseg = 0;
@@ -748,7 +787,6 @@ int kvtc_decompress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
       ret = KVTC_ECUDA;
     if (ret != KVTC_OK) break;
     if (tc > 0) {
-      std::memset(p, 0, sizeof(*p));
       int tiles = 0;
       for (size_t i = i0; i < i1; ++i) {
         const HostStream& h = c->hs[cs[i]];

@@ -31,6 +31,25 @@ struct DevStream {
   int32_t pad[2];
 };
 
+// Raw rows (sink and window) copied by two warps of a tensor-core kernel
+// while it runs: up to kRawListMax row segments; a segment whose src is
+// null writes zeros (stream padding).
+constexpr int kRawListMax = 192;
+struct RawListSeg {
+  const char* src;          // source row base, or null for zeros
+  char* dst;                // destination row base
+  int64_t src_ld, dst_ld;   // row strides in bytes
+  int32_t rows;             // rows to copy
+  int32_t row_bytes;        // bytes per row (multiple of 16)
+  int64_t chunk_begin;      // first 16-byte chunk index of this segment
+};
+struct RawList {
+  RawListSeg seg[kRawListMax];
+  int32_t nseg;
+  int32_t pad;
+  int64_t total_chunks;
+};
+
 // ---------------------------------------------------------------- compress
 constexpr int kCompMaxSeg = 64;
 struct CompSeg {
@@ -52,6 +71,7 @@ struct CompParams {
   int32_t stage_bytes;      // A + B bytes of one pipeline stage
   int32_t b_bytes_max;      // B bytes reserved per stage
   int32_t rec_stg_words;    // record staging words per thread
+  RawList raw;              // sink/window rows and padding of these streams
 };
 
 // -------------------------------------------------------------- decompress
@@ -73,7 +93,11 @@ struct DecParams {
   int32_t tiles_per_seg;    // every stream of a call has the same T
   int32_t nstages;          // B ring depth (shared-memory stages)
   int32_t rec_words;        // record staging words per thread (max R / 4)
+  RawList raw;              // sink/window rows of these streams
 };
+// every stream's sink, window and padding segments fit one launch's list
+static_assert(3 * kCompMaxSeg <= kRawListMax, "raw list too short");
+static_assert(2 * kDecMaxSeg <= kRawListMax, "raw list too short");
 
 // Paged restore: work items are (request, stream, tile).
 constexpr int kPagedMaxReq = 256;

@@ -125,10 +125,43 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Raw rows (sink and window, and zero padding) of a RawList, copied in
+// 16-byte chunks by the `stride` threads of the raw-copy role across the
+// grid (thread `tid` of them), four chunks in flight per thread.  Runs
+// beside the tensor-core work of the same kernel.
+__device__ __forceinline__ void raw_list_copy(const RawList& r, int64_t tid,
+                                              int64_t stride) {
+  int sg = 0;  // chunks visit increasing indices, so the segment only grows
+  for (int64_t c0 = tid; c0 < r.total_chunks; c0 += 4 * stride) {
+    uint4 v[4];
+    char* d[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t c = c0 + u * stride;
+      d[u] = nullptr;
+      v[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (c < r.total_chunks) {
+        while (sg + 1 < r.nseg && r.seg[sg + 1].chunk_begin <= c) ++sg;
+        const RawListSeg& g = r.seg[sg];
+        const int64_t cpr = g.row_bytes >> 4;
+        const int64_t local = c - g.chunk_begin;
+        const int64_t row = local / cpr;
+        const int64_t col = local - row * cpr;
+        if (g.src) v[u] = ld_nc_v4(g.src + row * g.src_ld + col * 16);
+        d[u] = g.dst + row * g.dst_ld + col * 16;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (d[u]) *reinterpret_cast<uint4*>(d[u]) = v[u];
+  }
+}
+
 // ======================================================================
 //                               decompress
 // ======================================================================
-constexpr int kDecWarps = 26;  // 0 TMA, 1 MMA, 2-9 prologue, 10-25 epilogue
+// 0 TMA, 1 MMA, 2-9 prologue, 10-25 epilogue, 26-27 raw rows
+constexpr int kDecWarps = 28;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kDecMaxNC = 256;  // widest output chunk (one MMA's N)
 constexpr int kDecMaxStages = 8;
@@ -523,6 +556,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
     KVTC_TR(0)
     KVTC_TR_SAVE(0)
     if (!ok && lane == 0) raise_abort(abort_flag, p.status);
+  } else if (warp >= 26) {
+    // ------------------------------- raw rows (sink and window) back
+    if constexpr (std::is_same<P, DecParams>::value)
+      raw_list_copy(p.raw, (int64_t)blockIdx.x * 64 + (warp - 26) * 32 + lane,
+                    (int64_t)gridDim.x * 64);
   } else {
     // -------------- epilogue: bf16 rows (the mean came in the MMA)
     // Sixteen warps.  With 256 / nc accumulators, 16 nc / 256 warps read
@@ -644,7 +682,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
 // ======================================================================
 //                                compress
 // ======================================================================
-constexpr int kCompWarps = 18;  // 0 TMA, 1 MMA, 2-17 epilogue (four sets)
+// 0 TMA, 1 MMA, 2-17 epilogue (four sets), 18-19 raw rows
+constexpr int kCompWarps = 20;
 constexpr int kCompThreads = kCompWarps * 32;
 constexpr int kCompMaxStages = 6;
 constexpr int kCompAStage = kTileM * 128;          // [128 rows][64 bf16]
@@ -828,6 +867,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
     }
     if (lane == 0) mbar_drain(mma_done, 0);
     __syncwarp();
+  } else if (warp >= 18) {
+    // ---------------------------- raw rows (sink, window) and padding
+    raw_list_copy(p.raw, (int64_t)blockIdx.x * 64 + (warp - 18) * 32 + lane,
+                  (int64_t)gridDim.x * 64);
   } else {
     // ------------------------- epilogue: quantise + bit-plane records
     // Four sets of four warps (one per TMEM lane quadrant each) share every
