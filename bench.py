@@ -383,6 +383,157 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_paged(args):
+    """Paged restore: every request's streams compressed once (untimed), then
+    kvtc_decompress_paged of all requests into 16-token blocks through the
+    seeded block table, timed.  The paged workload is decompress-only."""
+    import torch
+    import kv_cache_transform_gb300 as kv
+    from kv_cache_transform_gb300 import _build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    kv.lib()
+    w = synth.WORKLOADS[args.workload]
+    if args.layers:
+        import dataclasses
+        w = dataclasses.replace(w, layers=min(args.layers, w.layers))
+    streams = w.streams()
+    T, D, bs = w.tokens, w.D, w.block_size
+    stream = torch.cuda.current_stream()
+    t0 = time.perf_counter()
+    cal = [synth.calib_tokens_torch(w, l, k) for l, k in streams]
+    blob = kv.kvtc_calibrate(cal, [l for l, _ in streams],
+                             [k for _, k in streams], w.n_calib, D, D,
+                             w.sink, w.window, w.budget_bits, device=dev)
+    del cal
+    calib = kv.kvtc_calib_load(blob, dev)
+    calib_s = time.perf_counter() - t0
+    total = sum(calib.stream_bytes(l, k, T) for l, k in streams)
+    srcs = []
+    for r in range(w.requests):
+        x = [synth.eval_tokens_torch(w, l, k, request=r, T=T)
+             for l, k in streams]
+        comp = torch.empty(total, dtype=torch.uint8, device="cuda")
+        kv.kvtc_compress(calib, 0, w.layers, 3, x, D, T, comp, total, stream)
+        srcs.append(comp)
+        del x
+    table = synth.block_table(w)
+    nblocks = table.size
+    bt = torch.from_numpy(table).cuda()
+    caches = [torch.empty((nblocks, bs, D), dtype=torch.bfloat16,
+                          device="cuda") for _ in streams]
+    Ts = [T] * w.requests
+
+    def restore(src):
+        kv.kvtc_decompress_paged(calib, 0, w.layers, 3, src, Ts, bt,
+                                 table.shape[1], bs, caches, nblocks, stream)
+
+    for _ in range(max(3, args.warmup)):
+        restore(srcs)
+    torch.cuda.synchronize()
+    if kv.kvtc_device_status(calib):
+        raise RuntimeError("device flags after warm-up")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+          for _ in range(args.steps)]
+    launches0 = kv.kvtc_launch_count()
+    with ClockSampler(dev) as clocks:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            restore(srcs)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    launches = kv.kvtc_launch_count() - launches0
+    t_dec = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    (t_dec,) = max_over_ranks([t_dec], world, device="cuda")
+    flags = kv.kvtc_device_status(calib)
+    s_ = min(w.sink, T)
+    w_ = min(w.window, T - s_)
+    tc = T - s_ - w_
+    raw_kv = w.requests * len(streams) * T * D * 2
+    rec = w.requests * sum(tc * calib.query(l, k)["record_bytes"]
+                           for l, k in streams)
+    raw_rows = w.requests * len(streams) * (s_ + w_) * D * 2
+    dec_bytes = rec + raw_rows + raw_kv
+    flops = w.requests * sum(2 * D * calib.query(l, k)["k"] * tc
+                             for l, k in streams)
+    peaks, peak_kind = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    per = t_dec / args.steps
+    t_mem = dec_bytes / (hbm * 1e9)
+    roof = {"bound": "hbm", "achieved": dec_bytes / per / 1e9, "peak": hbm,
+            "unit": "GB/s", "frac": dec_bytes / per / 1e9 / hbm,
+            "traffic": None, "kernel": "decompress_paged",
+            "algorithmic_bytes": dec_bytes, "flops": flops,
+            "t_roof_us": 1e6 * max(t_mem, flops / (float(peaks["bf16_tflops"])
+                                                   * 1e12)),
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json burst)"}
+    # end to end: every request's compressed streams H2D from pinned host
+    # memory, the paged restore, the status word read back
+    host = [torch.empty(total, dtype=torch.uint8, pin_memory=True)
+            for _ in srcs]
+    for h, d in zip(host, srcs):
+        h.copy_(d)
+    torch.cuda.synchronize()
+    e2e_steps = max(2, min(args.steps, 5))
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        for h, d in zip(host, srcs):
+            d.copy_(h, non_blocking=True)
+        restore(srcs)
+        kv.kvtc_device_status(calib, stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = a.elapsed_time(b) / 1e3
+    line = {
+        "metric": METRIC,
+        "value": whole_job_gbs(world, raw_kv, args.steps, t_dec),
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * per,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(w) +
+                   f", {w.requests} requests, paged blocks of {bs}",
+                   "streams_per_request": len(streams), "tokens": T, "D": D,
+                   "k": sorted({calib.query(l, k)["k"] for l, k in streams}),
+                   "record_bytes": calib.query(0, 0)["record_bytes"],
+                   "l2": f"inputs larger than L2: {raw_kv / 1e9:.1f} GB out",
+                   "calibration_s": round(calib_s, 2)},
+        "decompress": {"value": whole_job_gbs(world, raw_kv, args.steps,
+                                              t_dec),
+                       "unit": "GB/s", "ms": 1e3 * per},
+        "roofline": roof,
+        "e2e": {"value": raw_kv * e2e_steps / t_e2e / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": total * len(srcs),
+                "d2h_bytes_per_step": 4},
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+        "device_flags": flags,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    calib.free()
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def run_layer_streaming(kv, torch, calib, w, comp, out, total, stream,
                         reps: int = 5):
     """Restore layer by layer (one launch per layer, an event after each)
@@ -466,7 +617,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=sorted(k for k, v in synth.WORKLOADS.items()
-                                   if v.requests == 1))
+                                   if v.requests == 1 or v.block_size))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="restrict to the first L layers (small profiling "
@@ -476,6 +627,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif synth.WORKLOADS[args.workload].block_size:
+        run_paged(args)
     else:
         run_ours(args)
 
