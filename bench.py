@@ -39,7 +39,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
 # of the kernel as it is now, per launch of the bench workload (a one-pass
 # capture of the full workload: profiles/launches_llama31_8b_8k.md); None
 # when the kernel has changed since the capture.
-NCU_TRAFFIC = {"decompress": 1091402496, "compress": 1145157632}
+NCU_TRAFFIC = {"decompress": 1125725696, "compress": 1181009664}
 
 
 def load_peaks():
