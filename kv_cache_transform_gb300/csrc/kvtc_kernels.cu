@@ -88,9 +88,36 @@ __device__ __forceinline__ void sts_u16(uint32_t addr, uint32_t v) {
                : "memory");
 }
 
-// Spread the 4 bits of n into bit 0 of each byte: bit m -> bit 8m.
-__device__ __forceinline__ uint32_t spread4(uint32_t n) {
-  return (n * 0x00204081u) & 0x01010101u;
+// 4-bit field of w at bit `pos` (one bfe).
+__device__ __forceinline__ uint32_t bfe4(uint32_t w, uint32_t pos) {
+  uint32_t r;
+  asm("bfe.u32 %0, %1, %2, 4;" : "=r"(r) : "r"(w), "r"(pos));
+  return r;
+}
+
+// Codes of one group from its B bit-planes (16 bits each, at byte offset po
+// of the staged record): w_n collects components 4n..4n+3, one code per
+// byte.  Plane j's nibble is spread straight to bit j of each byte (the
+// spread multiplier and mask shifted by j), so a nibble costs a bfe, a
+// multiply and one and-or.  (n * 0x00204081) & 0x01010101 moves bit m of a
+// nibble n to bit 8m: the four shifted copies 0, 7, 14, 21 never collide.
+template <int B>
+__device__ __forceinline__ void unpack_planes(const uint32_t* stg, int po,
+                                              int lane, uint32_t& w0,
+                                              uint32_t& w1, uint32_t& w2,
+                                              uint32_t& w3) {
+#pragma unroll
+  for (int j = 0; j < B; ++j) {
+    const int bo = po + 2 * j;
+    const uint32_t word = stg[(bo >> 2) * 33 + lane];
+    const uint32_t base = (uint32_t)(bo & 2) << 3;  // low or high half
+    const uint32_t mul = 0x00204081u << j;
+    const uint32_t mask = 0x01010101u << j;
+    w0 |= (bfe4(word, base) * mul) & mask;
+    w1 |= (bfe4(word, base + 4u) * mul) & mask;
+    w2 |= (bfe4(word, base + 8u) * mul) & mask;
+    w3 |= (bfe4(word, base + 12u) * mul) & mask;
+  }
 }
 
 // Gather bit 0 of each byte of x (x & 0x01010101) into bits 0..3.
@@ -473,6 +500,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       const DecTile t = resolve(p, item);
       const DevStream* ds = p.streams + t.cs;
       const int R = ds->R, Ga = ds->Ga;
+      // group widths and plane offsets: lane a holds group a's (Ga <= 15),
+      // broadcast per group by shuffle
+      const int my_b = lane < Ga ? (int)ds->bits[lane] : 0;
+      const int my_po = lane < Ga ? (int)ds->poff[lane] : 0;
       const int row0 = t.tile * kPairM + (int)rank * kTileM + q * 32;
       const int nvalid = min(max(t.tc - row0, 0), 32);
       const uint8_t* rbase = t.rec + (int64_t)row0 * R;
@@ -513,18 +544,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       const uint32_t a_tmem =
           tmem + ((uint32_t)(q * 32) << 16) + 256u + abuf * 128u;
       for (int a = 0; a < Ga; ++a) {
-        const int b = ds->bits[a];
-        const int po = ds->poff[a];
+        const int b = __shfl_sync(0xFFFFFFFFu, my_b, a);
+        const int po = __shfl_sync(0xFFFFFFFFu, my_po, a);
         const uint32_t f = stg[a * 33 + lane];
         uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
-        for (int j = 0; j < b; ++j) {
-          const int bo = po + 2 * j;
-          const uint32_t word = stg[(bo >> 2) * 33 + lane];
-          const uint32_t pl = (bo & 2) ? (word >> 16) : (word & 0xFFFFu);
-          w0 |= spread4(pl & 0xFu) << j;
-          w1 |= spread4((pl >> 4) & 0xFu) << j;
-          w2 |= spread4((pl >> 8) & 0xFu) << j;
-          w3 |= spread4((pl >> 12) & 0xFu) << j;
+        switch (b) {  // uniform over the warp
+          case 1: unpack_planes<1>(stg, po, lane, w0, w1, w2, w3); break;
+          case 2: unpack_planes<2>(stg, po, lane, w0, w1, w2, w3); break;
+          case 3: unpack_planes<3>(stg, po, lane, w0, w1, w2, w3); break;
+          case 4: unpack_planes<4>(stg, po, lane, w0, w1, w2, w3); break;
+          case 5: unpack_planes<5>(stg, po, lane, w0, w1, w2, w3); break;
+          case 6: unpack_planes<6>(stg, po, lane, w0, w1, w2, w3); break;
+          case 7: unpack_planes<7>(stg, po, lane, w0, w1, w2, w3); break;
+          default: unpack_planes<8>(stg, po, lane, w0, w1, w2, w3); break;
         }
         const __half2 sh2 =
             __half2half2(__ushort_as_half((unsigned short)(f & 0xFFFFu)));
