@@ -1,18 +1,22 @@
 // sm_103a kernels of the kvtc hot path.
 //
 //   compress   (kvtc page, technical summary 2B): c = V^T x - V^T mu on the
-//              5th-generation tensor cores (bf16 x bf16 -> fp32 in TMEM, both
-//              operands staged by TMA with the 128-byte swizzle), then a fused
-//              epilogue that quantises each 16-component group with its own
+//              5th-generation tensor cores (bf16 x bf16 -> fp32 in TMEM), run
+//              by CTA pairs (M = 256 over the pair) with x and V_enc staged
+//              by 3-D TMA boxes of two K blocks, then a fused epilogue of 16
+//              warps that quantises each 16-component group with its own
 //              fp16 shift/scale (microscaling, 2A) and writes bit-plane
 //              records with coalesced 16-byte stores.
 //   decompress (2C): a fused prologue unpacks the bit-planes and dequantises
 //              each group straight into an fp16 A operand held in TMEM; the
-//              tensor cores form V c_hat (fp16 x fp16 -> fp32) in 128-column
-//              chunks; the epilogue adds mu, rounds to bf16 and writes rows
-//              with bulk copies (contiguous or block-paged).
+//              tensor cores (CTA pairs, M = 256, N up to 256) form
+//              V c_hat + mu (the mean as one more K step) in fp32; the
+//              epilogue rounds to bf16 and writes rows with TMA tensor
+//              stores (contiguous) or 16-byte stores through the block table
+//              (paged).
 //   raw rows   (2A): attention-sink and recent-window rows are copied
-//              verbatim in 16-byte chunks.
+//              verbatim in 16-byte chunks, by two warps inside the tensor-core
+//              kernels (or a copy kernel when nothing is coded).
 //
 // Every mbarrier wait is bounded; a wait that runs out sets a sticky flag
 // and the CTA drains its own copies and MMAs, frees TMEM and returns.
