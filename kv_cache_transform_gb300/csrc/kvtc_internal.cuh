@@ -20,13 +20,14 @@ struct DevStream {
   CUtensorMap tm_vdec;      // fp16 [kb][D][64]: V_kept, then mu_hi, mu_lo,
                             // zeros (kp = k + 16 columns, padded to 64s),
                             // box {64, nc/2, kb}
-  CUtensorMap tm_venc;      // bf16 V_kept as [k rows][D cols], box {64, k/2}
+  CUtensorMap tm_venc;      // bf16 V_kept, K-block major [D/64][k][64],
+                            // box {64, k/2, 2}
   const float* mu;          // [D]   fp32 mean
   const float* m;           // [k]   fp32 projection of the mean
   const uint8_t* bits;      // [Ga]  width of each active group
   const uint16_t* poff;     // [Ga]  byte offset of the group's first plane
   int32_t D, k, Ga, R;      // R = record bytes
-  int32_t nc;               // reconstruction N chunk: 128 or 64
+  int32_t nc;               // reconstruction N chunk: 256, 128 or 64
   int32_t kp;               // reconstruction K: k + 16 (the mean step)
   int32_t pad[2];
 };
@@ -53,7 +54,8 @@ struct RawList {
 // ---------------------------------------------------------------- compress
 constexpr int kCompMaxSeg = 64;
 struct CompSeg {
-  CUtensorMap tm_x;         // bf16 rows [s'+T_c][D] of the source, box {64,128}
+  CUtensorMap tm_x;         // bf16 rows [s'+T_c][D] of the source viewed as
+                            // {64, rows, D/64}, box {64, 128, 2}
   uint8_t* rec;             // first record of the stream (device)
   int32_t tc;               // compressed tokens
   int32_t row0;             // s' (first compressed source row)
@@ -68,7 +70,7 @@ struct CompParams {
   int32_t total_tiles;
   int32_t tiles_per_seg;    // every stream of a call has the same T
   int32_t nstages;
-  int32_t stage_bytes;      // A + B bytes of one pipeline stage
+  int32_t stage_bytes;      // A + B bytes of one stage (two K blocks)
   int32_t b_bytes_max;      // B bytes reserved per stage
   int32_t rec_stg_words;    // record staging words per thread
   RawList raw;              // sink/window rows and padding of these streams

@@ -196,19 +196,21 @@ constexpr int kDecWarps = 28;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kDecMaxNC = 256;  // widest output chunk (one MMA's N)
 constexpr int kDecMaxStages = 8;
-// one B stage = this CTA's half of a chunk, every K block: [kb][64 rows][64]
+// one B stage = this CTA's half of a chunk, every K block: [kb][nc/2][64]
 constexpr int kDecBStage = (kDecMaxNC / 2) * 128 * (kMaxK / 64 + 1);
 constexpr int kDecStgWarp = 32 * 128;  // 32 rows x 64 bf16, SW128
 constexpr int kDecBarBytes = 512;
-// Shared memory: [B ring: nstages x 32 KB][staging: 16 warps x 4 KB]
-// [records: 8 warps x rec_words x 33 u32][barriers][misc]
+// Shared memory: [B ring: nstages x 64 KB][staging: 16 warps x 4 KB]
+// [records: 8 warps x rec_words x 33 u32][barriers][misc].  The ring is as
+// deep as fits: two stages for records up to 128 bytes, one (the B load of
+// the next chunk waits for the MMAs of this one) for longer records.
 int decompress_smem_bytes(int nstages, int rec_words) {
   return nstages * kDecBStage + 16 * kDecStgWarp + 8 * rec_words * 33 * 4 +
          kDecBarBytes + 64 + 1024;
 }
 int decompress_stages(int rec_words) {
   int n = kDecMaxStages;
-  while (n > 2 && decompress_smem_bytes(n, rec_words) > 232448) --n;
+  while (n > 1 && decompress_smem_bytes(n, rec_words) > 232448) --n;
   return n;
 }
 // TMEM columns: accumulators in [0, 256) (256 / nc of them, nc columns

@@ -83,6 +83,12 @@ WORKLOADS = {
                           head_dim=64, tokens=700, requests=1, rank=32,
                           spectrum_p=1.0, outliers=True, sink=4, window=16,
                           avg_bits=2.0),
+    # 10.42 bits per coefficient: every group at width 8, 256-byte records
+    # (the longest the format has)
+    "edge_d192_r256": Workload("edge_d192_r256", layers=1, kv=(0, 1),
+                               heads=3, head_dim=64, tokens=600, requests=1,
+                               rank=32, spectrum_p=1.0, outliers=True, sink=4,
+                               window=16, avg_bits=10.42),
     # flat spectrum and 2.5 bits: the DP keeps 15 groups (k = 240, the
     # widest the kernels take)
     "edge_d384": Workload("edge_d384", layers=2, kv=(0, 1), heads=3,

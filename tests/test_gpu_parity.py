@@ -128,6 +128,12 @@ def test_d192_64_column_chunks_odd_k_blocks(kv, torch):
     run_roundtrip(kv, torch, "edge_d192", [(0, 0), (0, 1)], 700)
 
 
+def test_d192_256_byte_records(kv, torch):
+    """Every group at width 8: 256-byte records, the longest the format has
+    (the decompress B ring drops to one stage to make room for them)."""
+    run_roundtrip(kv, torch, "edge_d192_r256", [(0, 0), (0, 1)], 600)
+
+
 def test_d384_128_column_chunks(kv, torch):
     """D = 384: three 128-column output chunks (two accumulators), k = 240
     (sixteen MMA K steps with the mean step, every predicated step on)."""
