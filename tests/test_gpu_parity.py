@@ -147,6 +147,13 @@ def test_llama_shape_several_streams_ragged(kv, torch):
     print(stats, dstats)
 
 
+def test_more_streams_than_one_launch_holds(kv, torch):
+    """100 streams in one call: compress splits them over two launches of at
+    most 64 streams, decompress over two of at most 96."""
+    streams = [(l, k) for l in range(50) for k in (0, 1)]
+    run_roundtrip(kv, torch, "llama33_70b_16k", streams, 400)
+
+
 def test_nemo_shape_k112(kv, torch):
     run_roundtrip(kv, torch, "mistral_nemo_12b_32k", [(0, 0), (0, 1)], 1500)
 
