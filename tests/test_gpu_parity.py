@@ -159,14 +159,23 @@ def test_nemo_shape_k112(kv, torch):
 
 
 def test_paged_restore_and_block_flag(kv, torch):
-    name = "qwen25_7b_paged"
+    run_paged(kv, torch, "qwen25_7b_paged", [(0, 0), (0, 1), (1, 0), (1, 1)],
+              [700, 37, 4096, 129])
+
+
+def test_paged_restore_256_byte_records(kv, torch):
+    """Paged restore with the longest records (one-stage B ring)."""
+    run_paged(kv, torch, "edge_d192_r256", [(0, 0), (0, 1)],
+              [600, 21, 300])
+
+
+def run_paged(kv, torch, name, streams, Ts):
     w = synth.WORKLOADS[name]
-    streams = [(0, 0), (0, 1), (1, 0), (1, 1)]
+    nl = max(l for l, _ in streams) + 1
     entries = calibrate_workload(name, streams)
     blob = blob_for(name, entries)
     scs = stream_calibs(blob)
     calib = kv.kvtc_calib_load(blob, 0)
-    Ts = [700, 37, 4096, 129]
     bs = 16
     maxb = -(-max(Ts) // bs)
     nblocks = len(Ts) * maxb + 7
@@ -184,9 +193,9 @@ def test_paged_restore_and_block_flag(kv, torch):
         oracle_bytes.append(parts)
         srcs.append(torch.from_numpy(np.frombuffer(b, np.uint8).copy()).cuda())
     caches = [torch.full((nblocks, bs, D), 0x7FC0, dtype=torch.int16,
-                         device="cuda") for _ in range(4)]
+                         device="cuda") for _ in range(2 * nl)]
     bt = torch.from_numpy(table).cuda()
-    kv.kvtc_decompress_paged(calib, 0, 2, 3, srcs, Ts, bt, maxb, bs, caches,
+    kv.kvtc_decompress_paged(calib, 0, nl, 3, srcs, Ts, bt, maxb, bs, caches,
                              nblocks)
     assert kv.kvtc_device_status(calib) == 0
     host = [from_dev(c) for c in caches]
@@ -208,9 +217,9 @@ def test_paged_restore_and_block_flag(kv, torch):
         assert np.all(c[free] == 0x7FC0)
     # an out-of-range block id is skipped and flagged, not a fault
     bad = table.copy()
-    bad[2, 5] = nblocks + 3
-    bad[3, 0] = -1
-    kv.kvtc_decompress_paged(calib, 0, 2, 3, srcs, Ts,
+    bad[-1, 1] = nblocks + 3
+    bad[0, 0] = -1
+    kv.kvtc_decompress_paged(calib, 0, nl, 3, srcs, Ts,
                              torch.from_numpy(bad).cuda(), maxb, bs, caches,
                              nblocks)
     assert kv.kvtc_device_status(calib) & kv.KVTC_FLAG_BLOCK
