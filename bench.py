@@ -570,7 +570,7 @@ def run_e2e(kv, torch, calib, w, comp, out, x, total, stream, steps):
     flags = torch.empty(1, dtype=torch.int32, pin_memory=True)
     raw_kv = len(x) * T * D * 2
     torch.cuda.synchronize()
-    # decompress direction
+    # decompress direction, serial: copy everything, then restore
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
@@ -578,6 +578,37 @@ def run_e2e(kv, torch, calib, w, comp, out, x, total, stream, steps):
         dev_comp.copy_(host_comp, non_blocking=True)
         kv.kvtc_decompress(calib, 0, w.layers, 3, dev_comp, total, T, out, D,
                            stream)
+        kv.kvtc_device_status(calib, stream)  # syncs, reads the flags back
+    b.record(stream)
+    torch.cuda.synchronize()
+    t_serial = a.elapsed_time(b) / 1e3
+    # decompress direction, pipelined: the streams of a group of layers are
+    # contiguous in the compressed buffer, so group g + 1 is copied on a
+    # second stream while group g is restored
+    ngroups = 4 if w.layers % 4 == 0 else 1
+    per = w.layers // ngroups
+    sizes = [sum(calib.stream_bytes(l, k, T) for k in w.kv)
+             for l in range(w.layers)]
+    offs = [0]
+    for sz in sizes:
+        offs.append(offs[-1] + sz)
+    copy_stream = torch.cuda.Stream()
+    evs = [torch.cuda.Event() for _ in range(ngroups)]
+    a.record(stream)
+    for _ in range(steps):
+        copy_stream.wait_event(a)
+        for g in range(ngroups):
+            l0, l1 = g * per, (g + 1) * per
+            with torch.cuda.stream(copy_stream):
+                dev_comp[offs[l0]:offs[l1]].copy_(
+                    host_comp[offs[l0]:offs[l1]], non_blocking=True)
+                evs[g].record(copy_stream)
+            stream.wait_event(evs[g])
+            nk = len(w.kv)
+            kv.kvtc_decompress(calib, l0, per, 3,
+                               dev_comp[offs[l0]:offs[l1]],
+                               offs[l1] - offs[l0], T,
+                               out[nk * l0:nk * l1], D, stream)
         kv.kvtc_device_status(calib, stream)  # syncs, reads the flags back
     b.record(stream)
     torch.cuda.synchronize()
@@ -602,6 +633,10 @@ def run_e2e(kv, torch, calib, w, comp, out, x, total, stream, steps):
     del flags
     return {"value": raw_kv * steps / t_dec / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": total, "d2h_bytes_per_step": 4,
+            "serial_value": raw_kv * steps / t_serial / 1e9,
+            "pipeline": f"{ngroups} groups of {per} layers: the H2D copy of a "
+                        "group on a second stream overlaps the restore of the "
+                        "previous one (serial_value: copy all, then restore)",
             "what": "restore: compressed streams H2D from pinned memory, "
                     "kvtc_decompress into device KV, status word read back",
             "compress": {"value": raw_kv * steps / t_comp / 1e9,
