@@ -283,6 +283,8 @@ def run_ours(args):
     launches = kv.kvtc_launch_count() - launches0
     t_comp = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
     t_dec = sum(e[1].elapsed_time(e[2]) for e in ev) / 1e3
+    med_comp = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    med_dec = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
     t_step = sum(e[0].elapsed_time(e[2]) for e in ev) / 1e3
     t_comp, t_dec, t_step = max_over_ranks([t_comp, t_dec, t_step], world,
                                            device="cuda")
@@ -353,10 +355,12 @@ def run_ours(args):
                    "calibration_s": round(calib_s, 2)},
         "compress": {"value": whole_job_gbs(world, raw_kv, args.steps, t_comp),
                      "unit": "GB/s", "ms": 1e3 * t_comp / args.steps,
+                     "ms_median": med_comp,
                      "compressed_out_gbs": world * (rec + raw_rows) *
                      args.steps / t_comp / 1e9},
         "decompress": {"value": whole_job_gbs(world, raw_kv, args.steps, t_dec),
                        "unit": "GB/s", "ms": 1e3 * t_dec / args.steps,
+                       "ms_median": med_dec,
                        "compressed_in_gbs": world * (rec + raw_rows) *
                        args.steps / t_dec / 1e9},
         "compression_ratio": raw_kv / total,
