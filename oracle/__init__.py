@@ -20,6 +20,9 @@ Modules:
                 compress / decompress / paged decompress.
   calibrate  -- PCA basis, measured distortion table, DP bit allocation,
                 calibration blob writer.
+  fieldpack  -- lossless field packing of a stream's records (the sign and
+                exponent of each fp16 field as an offset from the stream's
+                minimum), our stand-in for the page's entropy stage.
 
 Parity status: every function is pinned by ``tests/test_oracle_*.py``
 (brute force, closed forms, invariants, library special cases).  The one
