@@ -339,6 +339,8 @@ def run_ours(args):
     # raw KV from pinned host memory and the streams read back.
     e2e = run_e2e(kv, torch, calib, w, comp, out, x, total, stream,
                   max(3, args.steps // 2))
+    field_packing = run_fieldpack(kv, torch, calib, w, comp, out, total,
+                                  stream, max(3, args.steps // 4))
 
     line = {
         "metric": METRIC,
@@ -368,6 +370,7 @@ def run_ours(args):
         "rooflines": {"decompress": roof_dec, "compress": roof_comp},
         "e2e": e2e,
         "layer_streaming": layer_streaming,
+        "field_packing": field_packing,
         "gpu_launches": launches,
         "clocks": clocks.summary(),
         "device_flags": flags,
@@ -646,6 +649,121 @@ def run_e2e(kv, torch, calib, w, comp, out, x, total, stream, steps):
             "compress": {"value": raw_kv * steps / t_comp / 1e9,
                          "unit": "GB/s", "h2d_bytes_per_step": raw_kv,
                          "d2h_bytes_per_step": total}}
+
+
+def run_fieldpack(kv, torch, calib, w, comp, out, total, stream, steps):
+    """The lossless field-packing stage on the compressed streams: packed
+    size, pack and unpack throughput on the device, restore from packed
+    bytes (unpack, then decompress), and that restore end to end from pinned
+    host memory (the packed bytes of a group of layers copied on a second
+    stream while the previous group is restored)."""
+    T, D = w.tokens, w.D
+    streams = w.streams()
+    n = len(streams)
+    bound = kv.kvtc_fields_bound(calib, 0, w.layers, 3, T)
+    ws = kv.kvtc_fields_workspace_bytes(calib, 0, w.layers, 3)
+    packed = torch.empty(bound, dtype=torch.uint8, device="cuda")
+    offs = torch.empty(n + 1, dtype=torch.int64, device="cuda")
+    work = torch.empty(ws, dtype=torch.uint8, device="cuda")
+    back = torch.empty_like(comp)
+
+    def pack():
+        kv.kvtc_fields_pack(calib, 0, w.layers, 3, comp, total, T, packed,
+                            bound, offs, work, ws, stream)
+
+    def unpack(dst=back):
+        kv.kvtc_fields_unpack(calib, 0, w.layers, 3, packed, bound, offs, T,
+                              dst, total, stream)
+
+    for _ in range(3):
+        pack()
+        unpack()
+    torch.cuda.synchronize()
+    flags = kv.kvtc_device_status(calib)
+    if flags:
+        raise RuntimeError(f"device flags {flags} in field packing")
+    lossless = bool(torch.equal(back, comp))
+    ho = offs.cpu().numpy().astype(np.int64)
+    P = int(ho[-1])
+
+    def timed(fn):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 1e3 / steps
+
+    t_pack = timed(pack)
+    t_unpack = timed(unpack)
+
+    def restore():
+        unpack()
+        kv.kvtc_decompress(calib, 0, w.layers, 3, back, total, T, out, D,
+                           stream)
+
+    t_restore = timed(restore)
+    raw_kv = n * T * D * 2
+    peaks, _ = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    un_bytes = P + total
+
+    # end to end: packed bytes H2D in layer groups on a second stream
+    host_p = torch.empty(P, dtype=torch.uint8, pin_memory=True)
+    host_p.copy_(packed[:P])
+    dev_p = torch.empty(bound, dtype=torch.uint8, device="cuda")
+    dev_offs = offs.clone()
+    ngroups = 4 if w.layers % 4 == 0 else 1
+    per = w.layers // ngroups
+    nk = len(w.kv)
+    cs = [0]
+    for l in range(w.layers):
+        cs.append(cs[-1] + sum(calib.stream_bytes(l, k, T) for k in w.kv))
+    copy_stream = torch.cuda.Stream()
+    evs = [torch.cuda.Event() for _ in range(ngroups)]
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(steps):
+        copy_stream.wait_event(a)
+        for g in range(ngroups):
+            l0, l1 = g * per, (g + 1) * per
+            p0, p1 = int(ho[nk * l0]), int(ho[nk * l1])
+            with torch.cuda.stream(copy_stream):
+                dev_p[p0:p1].copy_(host_p[p0:p1], non_blocking=True)
+                evs[g].record(copy_stream)
+            stream.wait_event(evs[g])
+            kv.kvtc_fields_unpack(calib, l0, per, 3, dev_p, bound,
+                                  dev_offs[nk * l0:], T, back[cs[l0]:cs[l1]],
+                                  cs[l1] - cs[l0], stream)
+            kv.kvtc_decompress(calib, l0, per, 3, back[cs[l0]:cs[l1]],
+                               cs[l1] - cs[l0], T, out[nk * l0:nk * l1], D,
+                               stream)
+        kv.kvtc_device_status(calib, stream)  # syncs, reads the flags back
+    b.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = a.elapsed_time(b) / 1e3 / steps
+    return {
+        "lossless": lossless,
+        "codec_bytes": total, "packed_bytes": P,
+        "compression_ratio": raw_kv / P,
+        "saving": 1.0 - P / total,
+        "pack": {"ms": 1e3 * t_pack, "gbs": (total + P) / t_pack / 1e9},
+        "unpack": {"ms": 1e3 * t_unpack, "gbs": un_bytes / t_unpack / 1e9,
+                   "frac_of_hbm": un_bytes / t_unpack / 1e9 / hbm,
+                   "algorithmic_bytes": un_bytes},
+        "restore_from_packed": {"ms": 1e3 * t_restore,
+                                "value": raw_kv / t_restore / 1e9,
+                                "unit": "GB/s"},
+        "e2e_restore_from_packed": {
+            "value": raw_kv / t_e2e / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": P, "d2h_bytes_per_step": 4,
+            "pipeline": f"{ngroups} groups of {per} layers"},
+    }
 
 
 def main():

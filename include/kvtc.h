@@ -10,7 +10,8 @@
  *   decompress  (2C)  unpack, dequantise, x_hat = V c_hat + mu, bf16;
  *   sinks/window (2A) the first s and the last w tokens are stored raw.
  * The DEFLATE stage the page runs after packing (2B) is not part of this
- * library.
+ * library; an optional lossless field-packing stage of its own is
+ * (kvtc_fields_pack / kvtc_fields_unpack).
  *
  * Conventions for every entry point:
  *   - All device pointers are caller-owned CUDA device memory on the device
@@ -81,6 +82,7 @@ enum kvtc_status {
 #define KVTC_FLAG_RANGE 1u     /* a shift/scale left the fp16 range */
 #define KVTC_FLAG_TIMEOUT 2u   /* a bounded mbarrier wait ran out */
 #define KVTC_FLAG_BLOCK 4u     /* block-table id outside [0, num_blocks) */
+#define KVTC_FLAG_FORMAT 8u    /* packed stream inconsistent (field packing) */
 
 typedef struct kvtc_calib kvtc_calib;
 
@@ -169,6 +171,76 @@ int kvtc_decompress_paged(const kvtc_calib* calib, int layer0, int nlayers,
                           const int64_t* T, int R, const int32_t* block_table,
                           int max_blocks, int block_size, void* const* cache,
                           int64_t num_blocks, void* cuda_stream);
+
+/*
+ * Field packing -- a lossless stage after bit-packing.  The page runs DEFLATE
+ * there (technical summary 2B); this library runs a format of its own that
+ * targets the one redundant part of a record, the high byte of each fp16
+ * field.  Per stream and field slot (slot 2a = shift of active group a,
+ * 2a + 1 = its scale), v = high byte >> 2 (sign and exponent) is stored as
+ * v - vmin in dbits bits, vmin / dbits = the minimum and the bit length of
+ * the range of v over the stream's records (dbits <= 6); the other bits are
+ * kept, and the record's zero padding is dropped.
+ *
+ *   Packed stream (little-endian): header "KVFP", u32 T_c, u16 Rp (packed
+ *   record bytes), u16 nslot (= 2 G_a), u32 0; slot table nslot x (u8 vmin,
+ *   u8 dbits) zero-padded to 16-byte multiples; the s' + w' raw rows as in
+ *   the codec stream; T_c packed records of Rp bytes; zeros to a 256-byte
+ *   multiple.  Packed record: the low bytes of the 2 G_a fields in slot
+ *   order; the codes, per slot v - vmin in dbits bits then the high byte's
+ *   low 2 bits, least significant bit first, in 2 ceil(bits / 16) bytes;
+ *   the bit-planes of the codec record unchanged.  Rp <= the record's used
+ *   bytes, so a packed stream is never longer than the codec stream plus
+ *   its header and table.  Streams are concatenated in (layer, K, V) order.
+ */
+
+/* Upper bound on the packed bytes of the selected streams at T tokens
+ * (< 0 on error). */
+int64_t kvtc_fields_bound(const kvtc_calib* calib, int layer0, int nlayers,
+                          int kv_mask, int64_t T);
+
+/* Device workspace bytes kvtc_fields_pack needs (< 0 on error). */
+int64_t kvtc_fields_workspace_bytes(const kvtc_calib* calib, int layer0,
+                                    int nlayers, int kv_mask);
+
+/*
+ * kvtc_fields_pack -- pack codec streams.
+ *   src, src_bytes   : device codec streams as kvtc_compress wrote them
+ *                      (same layers, kv_mask and T).
+ *   dst, dst_capacity: device output, at least kvtc_fields_bound bytes; the
+ *                      packed streams are written back to back.
+ *   offsets          : device int64 [n + 1] (n = selected streams), written:
+ *                      packed stream i occupies [offsets[i], offsets[i+1])
+ *                      of dst; offsets[n] is the packed size.
+ *   workspace        : device scratch of kvtc_fields_workspace_bytes bytes,
+ *                      used only while the call's work runs on cuda_stream.
+ * Three kernel launches per 256 streams (a min/max pass, a layout pass that
+ * writes headers, tables and offsets, and the pack pass); no host
+ * synchronisation.  src, dst and workspace 16-byte aligned, offsets 8.
+ * Errors: EINVAL, ESIZE, EALIGN, ENOMEM, ECUDA.
+ */
+int kvtc_fields_pack(const kvtc_calib* calib, int layer0, int nlayers,
+                     int kv_mask, const void* src, int64_t src_bytes,
+                     int64_t T, void* dst, int64_t dst_capacity,
+                     int64_t* offsets, void* workspace,
+                     int64_t workspace_bytes, void* cuda_stream);
+
+/*
+ * kvtc_fields_unpack -- restore the codec streams that kvtc_fields_pack
+ * packed, byte for byte.
+ *   src, src_bytes : device packed streams.
+ *   offsets        : device int64 [n + 1] as kvtc_fields_pack wrote them.
+ *   dst, dst_bytes : device output, the codec streams (kvtc_stream_bytes
+ *                    each, concatenated as kvtc_compress writes them).
+ * Each stream's header and table are checked against its calibration, T
+ * and offsets on the GPU; a stream that does not match is skipped and flags
+ * KVTC_FLAG_FORMAT.  One kernel launch per 256 streams.
+ * Errors: EINVAL, ESIZE, EALIGN, ENOMEM, ECUDA.
+ */
+int kvtc_fields_unpack(const kvtc_calib* calib, int layer0, int nlayers,
+                       int kv_mask, const void* src, int64_t src_bytes,
+                       const int64_t* offsets, int64_t T, void* dst,
+                       int64_t dst_bytes, void* cuda_stream);
 
 /*
  * kvtc_calibrate -- the one-time calibration of technical summary 2A, on

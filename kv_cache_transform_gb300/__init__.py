@@ -6,7 +6,8 @@ mirror the C ABI in ``include/kvtc.h``:
 
     kvtc_calib_load, kvtc_calib_free, kvtc_calib_query, kvtc_stream_bytes,
     kvtc_compress, kvtc_decompress, kvtc_decompress_paged,
-    kvtc_device_status, kvtc_launch_count, kvtc_strerror
+    kvtc_fields_bound, kvtc_fields_workspace_bytes, kvtc_fields_pack,
+    kvtc_fields_unpack, kvtc_device_status, kvtc_launch_count, kvtc_strerror
 
 Tensor arguments are torch CUDA tensors (or raw integer device addresses);
 ``stream`` defaults to torch's current stream.  There is no CPU fallback: if
@@ -35,6 +36,7 @@ KVTC_ENOTSUP = -9
 KVTC_FLAG_RANGE = 1
 KVTC_FLAG_TIMEOUT = 2
 KVTC_FLAG_BLOCK = 4
+KVTC_FLAG_FORMAT = 8
 
 _lib_handle = None
 
@@ -83,6 +85,12 @@ def lib() -> ctypes.CDLL:
         "kvtc_calib_mean_static": (c_i, [c_i, c_vp, c_i64, c_i64, c_i, c_vp,
                                          c_vp]),
         "kvtc_wait_selftest": (c_i, [c_vp, ctypes.c_uint32, c_vp]),
+        "kvtc_fields_bound": (c_i64, [c_vp, c_i, c_i, c_i, c_i64]),
+        "kvtc_fields_workspace_bytes": (c_i64, [c_vp, c_i, c_i, c_i]),
+        "kvtc_fields_pack": (c_i, [c_vp, c_i, c_i, c_i, c_vp, c_i64, c_i64,
+                                   c_vp, c_i64, c_vp, c_vp, c_i64, c_vp]),
+        "kvtc_fields_unpack": (c_i, [c_vp, c_i, c_i, c_i, c_vp, c_i64, c_vp,
+                                     c_i64, c_vp, c_i64, c_vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -249,6 +257,45 @@ def kvtc_decompress_paged(calib: Calib, layer0: int, nlayers: int,
         calib.handle, layer0, nlayers, kv_mask, _ptr_array(src), Ts, len(T),
         _ptr(block_table) or None, max_blocks, block_size, _ptr_array(cache),
         num_blocks, _stream(stream) or None), "kvtc_decompress_paged")
+
+
+def kvtc_fields_bound(calib: Calib, layer0: int, nlayers: int,
+                      kv_mask: int, T: int) -> int:
+    return _check(lib().kvtc_fields_bound(calib.handle, layer0, nlayers,
+                                          kv_mask, T), "kvtc_fields_bound")
+
+
+def kvtc_fields_workspace_bytes(calib: Calib, layer0: int, nlayers: int,
+                                kv_mask: int) -> int:
+    return _check(lib().kvtc_fields_workspace_bytes(
+        calib.handle, layer0, nlayers, kv_mask),
+        "kvtc_fields_workspace_bytes")
+
+
+def kvtc_fields_pack(calib: Calib, layer0: int, nlayers: int, kv_mask: int,
+                     src, src_bytes: int, T: int, dst, dst_capacity: int,
+                     offsets, workspace, workspace_bytes: int,
+                     stream=None) -> None:
+    """Pack codec streams; offsets: device int64 [n + 1], written."""
+    _check(lib().kvtc_fields_pack(calib.handle, layer0, nlayers, kv_mask,
+                                  _ptr(src) or None, src_bytes, T,
+                                  _ptr(dst) or None, dst_capacity,
+                                  _ptr(offsets) or None,
+                                  _ptr(workspace) or None, workspace_bytes,
+                                  _stream(stream) or None),
+           "kvtc_fields_pack")
+
+
+def kvtc_fields_unpack(calib: Calib, layer0: int, nlayers: int,
+                       kv_mask: int, src, src_bytes: int, offsets, T: int,
+                       dst, dst_bytes: int, stream=None) -> None:
+    """Restore the codec streams of packed input (offsets as pack wrote)."""
+    _check(lib().kvtc_fields_unpack(calib.handle, layer0, nlayers, kv_mask,
+                                    _ptr(src) or None, src_bytes,
+                                    _ptr(offsets) or None, T,
+                                    _ptr(dst) or None, dst_bytes,
+                                    _stream(stream) or None),
+           "kvtc_fields_unpack")
 
 
 def kvtc_wait_selftest(calib: Calib, limit_us: int, stream=None) -> None:

@@ -15,7 +15,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
          "-I" + os.path.join(ROOT, "include")]
 SOURCES = ["kvtc_host.cu", "kvtc_kernels.cu", "kvtc_calib.cu",
-           "kvtc_static.cu"]
+           "kvtc_static.cu", "kvtc_fieldpack.cu"]
 LIBS = ["-lcublas", "-lcusolver"]
 DEPS = SOURCES + ["kvtc_internal.cuh", "ptx.cuh"]
 

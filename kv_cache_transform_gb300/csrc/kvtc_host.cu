@@ -918,6 +918,172 @@ int kvtc_decompress_paged(const kvtc_calib* c, int layer0, int nlayers,
   return ret;
 }
 
+// ------------------------------------------------------------ field packing
+namespace {
+
+// Used bytes of a codec record: per active group its two fp16 fields and
+// its b bit-planes of two bytes.
+int record_used(const HostStream& h) {
+  int u = 0;
+  for (uint8_t b : h.widths)
+    if (b) u += 4 + 2 * b;
+  return u;
+}
+
+int64_t fp_table_bytes_host(int ga) { return align_up(4LL * ga, 16); }
+
+// Worst-case packed bytes of one stream (every slot needing 6 offset bits
+// gives Rp = used bytes).
+int64_t fp_bound_of(const kvtc_calib* c, const HostStream& h, int64_t T) {
+  int64_t s_, w_, tc;
+  split_tokens(T, c->sink, c->window, &s_, &w_, &tc);
+  return align_up(kFpHeader + fp_table_bytes_host(h.Ga) +
+                      (s_ + w_) * h.D * 2 + tc * record_used(h),
+                  256);
+}
+
+// Fill the launch parameters of streams [i0, i1) of a field-packing call.
+void fp_fill(FpParams* p, const kvtc_calib* c, const std::vector<int>& cs,
+             const std::vector<int64_t>& codec_off, size_t i0, size_t i1,
+             int64_t T) {
+  std::memset(p, 0, sizeof(*p));
+  int64_t s_, w_, tc;
+  split_tokens(T, c->sink, c->window, &s_, &w_, &tc);
+  int items = 0;
+  for (size_t i = i0; i < i1; ++i) {
+    const HostStream& h = c->hs[cs[i]];
+    FpStream& f = p->s[i - i0];
+    f.in_off = codec_off[i];
+    f.out_off = codec_off[i];
+    f.raw_bytes = (s_ + w_) * h.D * 2;
+    f.tc = (int32_t)tc;
+    f.ntiles = (int32_t)((tc + kFpTile - 1) / kFpTile);
+    f.nraw = (int32_t)((f.raw_bytes + kFpRawChunk - 1) / kFpRawChunk);
+    f.ga = (int16_t)h.Ga;
+    f.used = (int16_t)record_used(h);
+    f.R = (int16_t)h.R;
+    f.item_begin = items;
+    items += f.ntiles + f.nraw;
+  }
+  p->n = (int32_t)(i1 - i0);
+  p->first = (int32_t)i0;
+  p->total_items = items;
+}
+
+}  // namespace
+
+int64_t kvtc_fields_bound(const kvtc_calib* c, int layer0, int nlayers,
+                          int kv_mask, int64_t T) {
+  if (!c || T < 0 || T > (1LL << 31) - 1) return KVTC_EINVAL;
+  std::vector<int> cs, slot;
+  const int st = select_streams(c, layer0, nlayers, kv_mask, &cs, &slot);
+  if (st != KVTC_OK) return st;
+  int64_t n = 0;
+  for (int i : cs) n += fp_bound_of(c, c->hs[i], T);
+  return n;
+}
+
+int64_t kvtc_fields_workspace_bytes(const kvtc_calib* c, int layer0,
+                                    int nlayers, int kv_mask) {
+  if (!c) return KVTC_EINVAL;
+  std::vector<int> cs, slot;
+  const int st = select_streams(c, layer0, nlayers, kv_mask, &cs, &slot);
+  if (st != KVTC_OK) return st;
+  const int64_t n = std::min<int64_t>((int64_t)cs.size(), kFpMaxStream);
+  return std::max<int64_t>(n, 1) * kFpChunks * kFpWorkWords * 4;
+}
+
+int kvtc_fields_pack(const kvtc_calib* c, int layer0, int nlayers,
+                     int kv_mask, const void* src, int64_t src_bytes,
+                     int64_t T, void* dst, int64_t dst_capacity,
+                     int64_t* offsets, void* workspace,
+                     int64_t workspace_bytes, void* cuda_stream) {
+  if (!c || !dst || !offsets || !workspace || T < 0 || T > (1LL << 31) - 1)
+    return KVTC_EINVAL;
+  std::vector<int> cs, slot;
+  int st = select_streams(c, layer0, nlayers, kv_mask, &cs, &slot);
+  if (st != KVTC_OK) return st;
+  if (cs.empty()) return KVTC_EINVAL;
+  std::vector<int64_t> off(cs.size());
+  int64_t need = 0, bound = 0;
+  for (size_t i = 0; i < cs.size(); ++i) {
+    off[i] = need;
+    need += stream_bytes_of(c, c->hs[cs[i]], T);
+    bound += fp_bound_of(c, c->hs[cs[i]], T);
+  }
+  if (!src && need) return KVTC_EINVAL;
+  if (src_bytes < need || dst_capacity < bound) return KVTC_ESIZE;
+  const int64_t ws = std::min<int64_t>((int64_t)cs.size(), kFpMaxStream) *
+                     kFpChunks * kFpWorkWords * 4;
+  if (workspace_bytes < ws) return KVTC_ESIZE;
+  if (!aligned16(src) || !aligned16(dst) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(offsets) & 7u))
+    return KVTC_EALIGN;
+  DeviceGuard guard(c->device);
+  if (!guard.ok) return KVTC_ECUDA;
+  FpParams* p = new (std::nothrow) FpParams;
+  if (!p) return KVTC_ENOMEM;
+  int ret = KVTC_OK;
+  for (size_t i0 = 0; i0 < cs.size() && ret == KVTC_OK; i0 += kFpMaxStream) {
+    const size_t i1 = std::min(cs.size(), i0 + (size_t)kFpMaxStream);
+    fp_fill(p, c, cs, off, i0, i1, T);
+    p->in = static_cast<const uint8_t*>(src);
+    p->out = static_cast<uint8_t*>(dst);
+    p->offsets = offsets;
+    p->work = static_cast<uint32_t*>(workspace);
+    p->status = c->d_status;
+    p->in_bytes = src_bytes;
+    if (launch_fields_pack(*p, static_cast<cudaStream_t>(cuda_stream)) !=
+        cudaSuccess)
+      ret = KVTC_ECUDA;
+  }
+  delete p;
+  return ret;
+}
+
+int kvtc_fields_unpack(const kvtc_calib* c, int layer0, int nlayers,
+                       int kv_mask, const void* src, int64_t src_bytes,
+                       const int64_t* offsets, int64_t T, void* dst,
+                       int64_t dst_bytes, void* cuda_stream) {
+  if (!c || !src || !offsets || T < 0 || T > (1LL << 31) - 1)
+    return KVTC_EINVAL;
+  std::vector<int> cs, slot;
+  int st = select_streams(c, layer0, nlayers, kv_mask, &cs, &slot);
+  if (st != KVTC_OK) return st;
+  if (cs.empty()) return KVTC_EINVAL;
+  std::vector<int64_t> off(cs.size());
+  int64_t need = 0;
+  for (size_t i = 0; i < cs.size(); ++i) {
+    off[i] = need;
+    need += stream_bytes_of(c, c->hs[cs[i]], T);
+  }
+  if (!dst && need) return KVTC_EINVAL;
+  if (dst_bytes < need) return KVTC_ESIZE;
+  if (src_bytes < (int64_t)cs.size() * 256) return KVTC_ESIZE;
+  if (!aligned16(src) || !aligned16(dst) ||
+      (reinterpret_cast<uintptr_t>(offsets) & 7u))
+    return KVTC_EALIGN;
+  DeviceGuard guard(c->device);
+  if (!guard.ok) return KVTC_ECUDA;
+  FpParams* p = new (std::nothrow) FpParams;
+  if (!p) return KVTC_ENOMEM;
+  int ret = KVTC_OK;
+  for (size_t i0 = 0; i0 < cs.size() && ret == KVTC_OK; i0 += kFpMaxStream) {
+    const size_t i1 = std::min(cs.size(), i0 + (size_t)kFpMaxStream);
+    fp_fill(p, c, cs, off, i0, i1, T);
+    p->in = static_cast<const uint8_t*>(src);
+    p->out = static_cast<uint8_t*>(dst);
+    p->offsets = const_cast<int64_t*>(offsets);
+    p->status = c->d_status;
+    p->in_bytes = src_bytes;
+    if (launch_fields_unpack(*p, static_cast<cudaStream_t>(cuda_stream)) !=
+        cudaSuccess)
+      ret = KVTC_ECUDA;
+  }
+  delete p;
+  return ret;
+}
+
 int kvtc_wait_selftest(const kvtc_calib* c, uint32_t limit_us,
                        void* cuda_stream) {
   if (!c || limit_us < 1 || limit_us > 2000000u) return KVTC_EINVAL;

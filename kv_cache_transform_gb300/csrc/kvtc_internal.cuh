@@ -146,6 +146,43 @@ struct RawParams {
   int64_t total_chunks;
 };
 
+// ----------------------------------------------------------- field packing
+// Lossless packing of codec streams (kvtc_fieldpack.cu).  Work of one launch
+// group: up to kFpMaxStream streams; items are per stream its raw-row
+// chunks then its record tiles.
+constexpr int kFpMaxStream = 256;
+constexpr int kFpChunks = 8;          // min/max partial results per stream
+constexpr int kFpWorkWords = 32;      // u32 words per (stream, chunk)
+constexpr int kFpTile = 128;          // tokens per pack / unpack tile
+constexpr int kFpRawChunk = 32768;    // raw-row bytes per copy item
+constexpr int kFpHeader = 16;         // packed stream header bytes
+struct FpStream {
+  int64_t in_off;       // pack: codec stream offset in the input
+  int64_t out_off;      // unpack: codec stream offset in the output
+  int64_t raw_bytes;    // (s' + w') * D * 2
+  int32_t tc;           // compressed tokens
+  int32_t item_begin;   // first work item of this stream
+  int32_t ntiles;       // ceil(tc / kFpTile)
+  int32_t nraw;         // ceil(raw_bytes / kFpRawChunk)
+  int16_t ga;           // active groups
+  int16_t used;         // used bytes of a codec record
+  int16_t R;            // codec record bytes
+  int16_t pad;
+};
+struct FpParams {
+  FpStream s[kFpMaxStream];
+  const uint8_t* in;
+  uint8_t* out;
+  int64_t* offsets;     // packed stream offsets [all streams + 1]
+  uint32_t* work;       // pack: min/max partials [n][kFpChunks][32]
+  unsigned* status;
+  int64_t in_bytes;     // unpack: bytes of the packed input
+  int32_t n;            // streams of this launch group
+  int32_t first;        // index of its first stream in offsets
+  int32_t total_items;
+  int32_t pad;
+};
+
 // Launchers (kvtc_kernels.cu).  Return a cudaError_t.
 // `pairs`: CTA pairs to launch (each kernel runs as clusters of two).
 cudaError_t launch_compress(const CompParams& p, int pairs, cudaStream_t st);
@@ -159,6 +196,9 @@ cudaError_t launch_raw_copy(const RawParams& p, cudaStream_t st);
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns,
                                  cudaStream_t st);
 cudaError_t launch_paged_raw(const PagedParams& p, cudaStream_t st);
+// Field packing (kvtc_fieldpack.cu): the three pack launches, and unpack.
+cudaError_t launch_fields_pack(const FpParams& p, cudaStream_t st);
+cudaError_t launch_fields_unpack(const FpParams& p, cudaStream_t st);
 // Kernel launches issued by this library (all devices, all threads).
 void count_launch();
 // CRC-32 of IEEE 802.3 (as zlib): reflected 0xEDB88320, init/final ~0.

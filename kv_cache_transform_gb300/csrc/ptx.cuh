@@ -208,6 +208,17 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// Bulk (non-tensor) copy global -> this CTA's shared memory, completing on
+// an mbarrier of this CTA (addresses 16-byte aligned, bytes % 16 == 0).
+__device__ __forceinline__ void bulk_g2s(void* sdst, const void* gsrc,
+                                         uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], "
+      "[%1], %2, [%3];" ::"r"(smem_u32(sdst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Bulk (non-tensor) copy shared -> global, tracked by a per-thread group.
 __device__ __forceinline__ void bulk_s2g(void* gdst, const void* ssrc,
                                          uint32_t bytes) {

@@ -101,6 +101,12 @@ def test_null_handles_are_rejected(kv):
     flags = ctypes.c_uint()
     assert L.kvtc_device_status(None, None, ctypes.byref(flags)) == \
         kv.KVTC_EINVAL
+    assert L.kvtc_fields_bound(None, 0, 1, 1, 10) == kv.KVTC_EINVAL
+    assert L.kvtc_fields_workspace_bytes(None, 0, 1, 1) == kv.KVTC_EINVAL
+    assert L.kvtc_fields_pack(None, 0, 1, 1, None, 0, 10, None, 0, None,
+                              None, 0, None) == kv.KVTC_EINVAL
+    assert L.kvtc_fields_unpack(None, 0, 1, 1, None, 0, None, 10, None, 0,
+                                None) == kv.KVTC_EINVAL
     L.kvtc_calib_free(None)  # no-op
 
 
