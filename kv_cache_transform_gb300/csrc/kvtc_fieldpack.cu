@@ -15,18 +15,18 @@
 //                     the packed record size Rp and stream size; an
 //                     exclusive scan gives the stream offsets; headers,
 //                     tables and offsets are written;
-//   fp_pack_kernel    persistent: raw-row chunks are copied, record tiles of
-//                     128 tokens are bulk-loaded into shared memory, one
-//                     warp packs one token at a time (lane s = field slot s,
-//                     the slots' codes merged with warp OR-reductions), and
-//                     the tile is bulk-stored.
-// Unpack is one persistent kernel of the same shape that checks each
-// stream's header against its calibration and offsets, then reverses the
-// tile transform.
+//   fp_tile_kernel<true>  persistent: raw-row chunks are copied, record
+//                     tiles of up to 32 KB are bulk-loaded into shared
+//                     memory, one warp packs one token at a time (lane s =
+//                     field slot s, the slots' codes merged with warp
+//                     OR-reductions), and the tile is bulk-stored.
+// Unpack is fp_tile_kernel<false>, the same pipeline, which checks each
+// stream's header against its calibration and offsets and then reverses
+// the tile transform.
 //
-// Both tile kernels are HBM-bound byte shuffles; the per-token work is a
-// few dozen instructions per warp, hidden behind three resident blocks per
-// SM.
+// Both directions are HBM-bound byte shuffles: the per-token work is a few
+// dozen instructions per warp, and each block keeps two 32 KB loads in
+// flight ahead of the tile it transforms.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -44,9 +44,8 @@ constexpr int kFpThreads = 256;
 constexpr int kFpWarps = kFpThreads / 32;
 constexpr int kFpLayoutThreads = 1024;
 constexpr uint32_t kFpMagic = 0x5046564Bu;  // "KVFP", little-endian
-constexpr int kFpInBytes = kFpTile * kMaxRecord;
-constexpr int kFpOutBytes = kFpTile * kMaxRecord + 256;
-constexpr int kFpSmem = kFpInBytes + kFpOutBytes + 16;  // + read slack
+constexpr int kFpBuf = kFpRawChunk;              // one input buffer
+constexpr int kFpSmem = 3 * kFpBuf + 256 + 16;   // 2 in, 1 out + padding
 
 __device__ __forceinline__ int fp_table_bytes(int ga) {
   return (4 * ga + 15) & ~15;
@@ -71,19 +70,6 @@ __device__ __forceinline__ int fp_find_stream(const FpParams& p, int item) {
     if (p.s[mid].item_begin <= item) lo = mid; else hi = mid - 1;
   }
   return lo;
-}
-
-// Copy bytes [b0, b1) (16-byte multiples) with the whole block.
-__device__ __forceinline__ void fp_block_copy(uint8_t* dst, const uint8_t* src,
-                                              int64_t bytes) {
-  const int64_t n = bytes >> 4;
-  for (int64_t c = threadIdx.x; c < n; c += blockDim.x)
-    reinterpret_cast<uint4*>(dst)[c] = ldg_nc(src + 16 * c);
-}
-__device__ __forceinline__ void fp_block_zero(uint8_t* dst, int64_t bytes) {
-  const int64_t n = bytes >> 4;
-  for (int64_t c = threadIdx.x; c < n; c += blockDim.x)
-    reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
 }
 
 // Per-lane slot description: lane s < 2 G_a holds slot s's vmin, dbits and
@@ -276,245 +262,369 @@ __global__ void __launch_bounds__(kFpLayoutThreads) fp_layout_kernel(
   }
 }
 
-// ------------------------------------------------------------- pack pass 3
-__global__ void __launch_bounds__(kFpThreads, 3) fp_pack_kernel(
+// ---------------------------------------------------- pack pass 3, unpack
+// One persistent kernel for both directions.  Block b takes a contiguous
+// range of work items; warp 0 resolves items (the stream's header is read
+// once per stream) and bulk-loads each into one of two input buffers two
+// items ahead of the block; all warps then transform a record tile into the
+// output buffer and one thread bulk-stores it.  A raw-row chunk goes out of
+// its input buffer unchanged.
+struct FpInfo {
+  const uint8_t* gsrc;    // bulk-load source
+  uint8_t* gdst;          // bulk-store destination
+  uint8_t* zero_dst;      // stream padding to clear after raw rows (or null)
+  int32_t kind;           // 0 skip, 1 raw chunk, 2 record tile
+  int32_t load_bytes;
+  int32_t store_bytes;    // tile: packed / codec bytes plus trailing padding
+  int32_t zero_bytes;
+  int32_t ntok, ga, used, R, rp, hb2;
+  uint16_t table[32];     // slot s: vmin | dbits << 8
+};
+
+template <bool kPack>
+__global__ void __launch_bounds__(kFpThreads, 2) fp_tile_kernel(
     const __grid_constant__ FpParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* s_in = smem;
-  uint8_t* s_out = smem + kFpInBytes;
-  __shared__ uint64_t bar;
+  uint8_t* s_out = smem + 2 * kFpBuf;
+  __shared__ uint64_t full[2];
+  __shared__ FpInfo info[2];
   __shared__ int abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nb = gridDim.x, bid = blockIdx.x;
+  const int q = p.total_items / nb, r = p.total_items % nb;
+  const int ib = bid * q + min(bid, r);
+  const int ie = ib + q + (bid < r ? 1 : 0);
   if (tid == 0) {
-    mbar_init(&bar, 1);
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
     abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
-  uint32_t phase = 0;
-  bool bad = false;
-  for (int item = blockIdx.x; item < p.total_items; item += gridDim.x) {
-    const int i = fp_find_stream(p, item);
+
+  // ---- producer state (warp 0): the stream whose header it holds
+  int c_i = -1, c_rp = 0, c_hb2 = 0;
+  int64_t c_off = 0, c_end = 0;
+  bool c_ok = false;
+  uint32_t c_tab = 0;
+  auto produce = [&](int j, int bsel) {
+    const int i = fp_find_stream(p, j);
     const FpStream& S = p.s[i];
-    const int local = item - S.item_begin;
-    const int ga = S.ga, tb = fp_table_bytes(ga);
-    const int64_t off = p.offsets[p.first + i];
-    const int64_t end = p.offsets[p.first + i + 1];
-    uint8_t* body = p.out + off + kFpHeader + tb;  // raw rows, then records
-    if (local < S.nraw) {
+    const int ga = S.ga, nslot = 2 * ga, tb = fp_table_bytes(ga);
+    if (i != c_i) {
+      c_i = i;
+      c_off = p.offsets[p.first + i];
+      c_end = p.offsets[p.first + i + 1];
+      const uint8_t* hbase = kPack ? p.out : p.in;
+      // unpack: read the header only once the offsets are known to frame it
+      c_ok = kPack || (c_off >= 0 && (c_off & 15) == 0 &&
+                       c_end <= p.in_bytes && c_end - c_off >= kFpHeader + tb);
+      int vmin = 0, d = 0;
+      c_tab = 0;
+      if (c_ok) {
+        if (lane < nslot) {
+          c_tab = reinterpret_cast<const uint16_t*>(hbase + c_off +
+                                                    kFpHeader)[lane];
+          vmin = c_tab & 0xff;
+          d = c_tab >> 8;
+        }
+        const FpSlots sl = fp_slots_from(vmin, d, nslot);
+        c_hb2 = (sl.hbits + 15) >> 4;
+        c_rp = 2 * ga + 2 * c_hb2 + (S.used - 4 * ga);
+        if (!kPack) {
+          const uint32_t* h = reinterpret_cast<const uint32_t*>(p.in + c_off);
+          const uint32_t h0 = h[0], h1 = h[1], h2 = h[2];
+          const bool slot_ok = lane >= nslot || (d <= 6 && vmin <= 63);
+          c_ok = __all_sync(0xffffffffu, slot_ok) && h0 == kFpMagic &&
+                 h1 == (uint32_t)S.tc && (h2 & 0xffffu) == (uint32_t)c_rp &&
+                 (h2 >> 16) == (uint32_t)nslot &&
+                 c_end - c_off == fp_align256(kFpHeader + tb + S.raw_bytes +
+                                              (int64_t)S.tc * c_rp);
+          if (!c_ok && lane == 0) atomicOr(p.status, KVTC_FLAG_FORMAT);
+        }
+      }
+    }
+    const int local = j - S.item_begin;
+    // byte positions of this stream in the packed and the codec buffers
+    const int64_t pbody = c_off + kFpHeader + tb;    // raw rows, then records
+    const int64_t cbody = kPack ? S.in_off : S.out_off;
+    const int64_t cend = cbody + fp_align256(S.raw_bytes + (int64_t)S.tc * S.R);
+    const uint8_t* pin = p.in;
+    uint8_t* pout = p.out;
+    FpInfo inf;
+    inf.zero_dst = nullptr;
+    inf.zero_bytes = 0;
+    inf.ntok = 0;
+    inf.ga = ga;
+    inf.used = S.used;
+    inf.R = S.R;
+    inf.rp = c_rp;
+    inf.hb2 = c_hb2;
+    if (!c_ok) {
+      inf.kind = 0;
+      inf.load_bytes = inf.store_bytes = 0;
+      inf.gsrc = nullptr;
+      inf.gdst = nullptr;
+    } else if (local < S.nraw) {
       const int64_t b0 = (int64_t)local * kFpRawChunk;
       const int64_t b1 = min(S.raw_bytes, b0 + kFpRawChunk);
-      fp_block_copy(body + b0, p.in + S.in_off + b0, b1 - b0);
-      if (S.tc == 0 && local == S.nraw - 1)
-        fp_block_zero(body + S.raw_bytes, end - (off + kFpHeader + tb) -
-                                              S.raw_bytes);
-      continue;
+      inf.kind = 1;
+      inf.load_bytes = inf.store_bytes = (int32_t)(b1 - b0);
+      inf.gsrc = kPack ? pin + cbody + b0 : pin + pbody + b0;
+      inf.gdst = kPack ? pout + pbody + b0 : pout + cbody + b0;
+      if (S.tc == 0 && local == S.nraw - 1) {
+        inf.zero_dst = kPack ? pout + pbody + S.raw_bytes
+                             : pout + cbody + S.raw_bytes;
+        inf.zero_bytes = kPack ? (int32_t)(c_end - pbody - S.raw_bytes)
+                               : (int32_t)(cend - cbody - S.raw_bytes);
+      }
+    } else {
+      const int tile = local - S.nraw;
+      const int t0 = tile * S.tile;
+      const int ntok = min((int)S.tile, S.tc - t0);
+      const int64_t prec = pbody + S.raw_bytes + (int64_t)t0 * c_rp;
+      const int64_t crec = cbody + S.raw_bytes + (int64_t)t0 * S.R;
+      const bool last = tile == S.ntiles - 1;
+      inf.kind = 2;
+      inf.ntok = ntok;
+      if (kPack) {
+        inf.gsrc = pin + crec;
+        inf.load_bytes = ntok * S.R;
+        inf.gdst = pout + prec;
+        inf.store_bytes = last ? (int32_t)(c_end - prec) : ntok * c_rp;
+      } else {
+        inf.gsrc = pin + prec;
+        inf.load_bytes = (ntok * c_rp + 15) & ~15;
+        inf.gdst = pout + crec;
+        inf.store_bytes = last ? (int32_t)(cend - crec) : ntok * S.R;
+      }
     }
-    const int tile = local - S.nraw;
-    const int t0 = tile * kFpTile;
-    const int ntok = min(kFpTile, S.tc - t0);
-    const int R = S.R, nslot = 2 * ga;
-    // slot table from this stream's header (written by the layout pass)
-    int vmin = 0, d = 0;
-    if (lane < nslot) {
-      const uint16_t e =
-          reinterpret_cast<const uint16_t*>(p.out + off + kFpHeader)[lane];
-      vmin = e & 0xff;
-      d = e >> 8;
+    uint16_t tab[32];
+#pragma unroll
+    for (int s = 0; s < 32; ++s)
+      tab[s] = (uint16_t)__shfl_sync(0xffffffffu, c_tab, s);
+    if (lane == 0) {
+      FpInfo& f = info[bsel];
+      f.gsrc = inf.gsrc;
+      f.gdst = inf.gdst;
+      f.zero_dst = inf.zero_dst;
+      f.kind = inf.kind;
+      f.load_bytes = inf.load_bytes;
+      f.store_bytes = inf.store_bytes;
+      f.zero_bytes = inf.zero_bytes;
+      f.ntok = inf.ntok;
+      f.ga = inf.ga;
+      f.used = inf.used;
+      f.R = inf.R;
+      f.rp = inf.rp;
+      f.hb2 = inf.hb2;
+#pragma unroll
+      for (int s = 0; s < 32; ++s) f.table[s] = tab[s];
+      if (inf.kind == 0) {
+        mbar_arrive(&full[bsel]);
+      } else {
+        mbar_arrive_expect_tx(&full[bsel], (uint32_t)inf.load_bytes);
+        bulk_g2s(smem + bsel * kFpBuf, inf.gsrc, (uint32_t)inf.load_bytes,
+                 &full[bsel]);
+      }
     }
-    const FpSlots sl = fp_slots_from(vmin, d, nslot);
-    const int hb2 = (sl.hbits + 15) >> 4;
-    const int rp = 2 * ga + 2 * hb2 + (S.used - 4 * ga);
-    const int p2 = (S.used - 4 * ga) >> 1;
-    const int nw = (sl.hbits + 31) >> 5;
-    uint8_t* gdst = body + S.raw_bytes + (int64_t)t0 * rp;
-    const int len = tile == S.ntiles - 1 ? (int)(p.out + end - gdst)
-                                         : ntok * rp;
-    // the previous tile's store has read s_out; everyone is done with s_in
-    if (tid == 0) bulk_wait_read<0>();
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      const uint32_t bytes = (uint32_t)(ntok * R);
-      mbar_arrive_expect_tx(&bar, bytes);
-      bulk_g2s(s_in, p.in + S.in_off + S.raw_bytes + (int64_t)t0 * R, bytes,
-               &bar);
-    }
-    for (int b = ntok * rp + tid; b < len; b += kFpThreads) s_out[b] = 0;
-    const bool ok = mbar_wait(&bar, phase, &abort_flag);
-    phase ^= 1u;
-    if (__syncthreads_or(!ok)) {
+    __syncwarp();
+  };
+
+  if (warp == 0) {
+    if (ib < ie) produce(ib, 0);
+    if (ib + 1 < ie) produce(ib + 1, 1);
+  }
+  uint32_t phase = 0;  // bit b: parity to wait for on full[b]
+  bool bad = false;
+  for (int it = ib; it < ie; ++it) {
+    const int bsel = (it - ib) & 1;
+    const bool got = mbar_wait(&full[bsel], (phase >> bsel) & 1u, &abort_flag);
+    phase ^= 1u << bsel;
+    if (__syncthreads_or(!got)) {
       if (tid == 0) {
         atomicOr(p.status, KVTC_FLAG_TIMEOUT);
-        mbar_drain(&bar, phase ^ 1u);
+        mbar_drain(&full[bsel], ((phase >> bsel) & 1u) ^ 1u);
+        if (it + 1 < ie)
+          mbar_drain(&full[bsel ^ 1], (phase >> (bsel ^ 1)) & 1u);
       }
       break;
     }
-    for (int tok = warp; tok < ntok; tok += kFpWarps) {
-      const uint32_t* in32 = reinterpret_cast<const uint32_t*>(s_in + tok * R);
-      uint8_t* ob = s_out + tok * rp;
-      uint16_t* o16 = reinterpret_cast<uint16_t*>(ob);
-      uint32_t clo = 0, chi = 0;
-      int w0 = -2;
+    const FpInfo& f = info[bsel];
+    const int kind = f.kind;
+    uint8_t* s_in = smem + bsel * kFpBuf;
+    if (kind == 2) {
+      const int ntok = f.ntok, ga = f.ga, nslot = 2 * ga, R = f.R;
+      const int rp = f.rp, hb2 = f.hb2, used = f.used;
+      const int store_bytes = f.store_bytes;
+      int vmin = 0, d = 0;
       if (lane < nslot) {
-        const uint32_t w = in32[lane >> 1];
-        const int sh = 16 * (lane & 1);
-        const uint32_t lo = (w >> sh) & 0xffu, hi = (w >> (sh + 8)) & 0xffu;
-        ob[lane] = (uint8_t)lo;
-        const int u = (int)(hi >> 2) - sl.vmin;
-        if (u < 0 || u >= (1 << sl.d)) bad = true;
-        const uint32_t code = ((uint32_t)u & ((1u << sl.d) - 1)) |
-                              ((hi & 3u) << sl.d);
-        w0 = sl.pos >> 5;
-        const int s5 = sl.pos & 31;
-        clo = code << s5;
-        chi = s5 ? code >> (32 - s5) : 0u;
+        vmin = f.table[lane] & 0xff;
+        d = f.table[lane] >> 8;
       }
-      uint32_t mine = 0;
+      const FpSlots sl = fp_slots_from(vmin, d, nslot);
+      if (tid == 0) bulk_wait_read<0>();  // s_out read by the last store
+      __syncthreads();
+      const int body = kPack ? ntok * rp : ntok * R;
+      for (int b = body + tid; b < store_bytes; b += kFpThreads) s_out[b] = 0;
+      if (kPack) {
+        // four tokens per warp step: their loads issue back to back
+        const int nw = (sl.hbits + 31) >> 5, p2 = (used - 4 * ga) >> 1;
+        const int w0 = lane < nslot ? sl.pos >> 5 : -2;
+        const int s5 = sl.pos & 31, fsh = 16 * (lane & 1);
+        const uint32_t umask = (1u << sl.d) - 1;
+        for (int tok0 = 4 * warp; tok0 < ntok; tok0 += 4 * kFpWarps) {
+          const int nt = min(4, ntok - tok0);
+          uint32_t wv[4], clo[4], chi[4], mine[4];
 #pragma unroll
-      for (int w = 0; w < 8; ++w) {
-        if (w < nw) {
-          const uint32_t v = __reduce_or_sync(
-              0xffffffffu, (w0 == w ? clo : 0u) | (w0 + 1 == w ? chi : 0u));
-          if ((lane >> 1) == w) mine = v;
+          for (int u = 0; u < 4; ++u)
+            wv[u] = (u < nt && lane < nslot)
+                        ? reinterpret_cast<const uint32_t*>(
+                              s_in + (tok0 + u) * R)[lane >> 1]
+                        : 0u;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            clo[u] = chi[u] = mine[u] = 0u;
+            if (u < nt && lane < nslot) {
+              const uint32_t lo = (wv[u] >> fsh) & 0xffu;
+              const uint32_t hi = (wv[u] >> (fsh + 8)) & 0xffu;
+              s_out[(tok0 + u) * rp + lane] = (uint8_t)lo;
+              const int v = (int)(hi >> 2) - sl.vmin;
+              if (v < 0 || v > (int)umask) bad = true;
+              const uint32_t code = ((uint32_t)v & umask) | ((hi & 3u) << sl.d);
+              clo[u] = code << s5;
+              chi[u] = s5 ? code >> (32 - s5) : 0u;
+            }
+          }
+#pragma unroll
+          for (int w = 0; w < 8; ++w) {
+            if (w < nw) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const uint32_t v = __reduce_or_sync(
+                    0xffffffffu,
+                    (w0 == w ? clo[u] : 0u) | (w0 + 1 == w ? chi[u] : 0u));
+                if ((lane >> 1) == w) mine[u] = v;
+              }
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (u < nt && lane < hb2)
+              reinterpret_cast<uint16_t*>(s_out + (tok0 + u) * rp)[ga + lane] =
+                  (uint16_t)(mine[u] >> fsh);
+          for (int j = lane; j < p2; j += 32) {
+            uint16_t v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              v[u] = u < nt ? reinterpret_cast<const uint16_t*>(
+                                  s_in + (tok0 + u) * R)[2 * ga + j]
+                            : (uint16_t)0;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (u < nt)
+                reinterpret_cast<uint16_t*>(
+                    s_out + (tok0 + u) * rp)[ga + hb2 + j] = v[u];
+          }
+        }
+      } else {
+        const int R2 = R >> 1, u2 = used >> 1;
+        const int k = sl.pos >> 4, sh = sl.pos & 15;
+        const uint32_t cmask = (4u << sl.d) - 1, umask = (1u << sl.d) - 1;
+        for (int tok0 = 4 * warp; tok0 < ntok; tok0 += 4 * kFpWarps) {
+          const int nt = min(4, ntok - tok0);
+          uint32_t bits[4], lob[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            bits[u] = lob[u] = 0u;
+            if (u < nt && lane < nslot) {
+              const uint8_t* ibp = s_in + (tok0 + u) * rp;
+              const uint16_t* i16 = reinterpret_cast<const uint16_t*>(ibp);
+              bits[u] = (uint32_t)i16[ga + k] | ((uint32_t)i16[ga + k + 1] << 16);
+              lob[u] = ibp[lane];
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (u < nt && lane < nslot) {
+              const uint32_t code = (bits[u] >> sh) & cmask;
+              const uint32_t hi =
+                  ((((code & umask) + sl.vmin) << 2) | (code >> sl.d)) & 0xffu;
+              reinterpret_cast<uint16_t*>(s_out + (tok0 + u) * R)[lane] =
+                  (uint16_t)(lob[u] | (hi << 8));
+            }
+          }
+          for (int j = 2 * ga + lane; j < R2; j += 32) {
+            uint16_t v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              v[u] = (u < nt && j < u2)
+                         ? reinterpret_cast<const uint16_t*>(
+                               s_in + (tok0 + u) * rp)[hb2 - ga + j]
+                         : (uint16_t)0;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (u < nt)
+                reinterpret_cast<uint16_t*>(s_out + (tok0 + u) * R)[j] = v[u];
+          }
         }
       }
-      if (lane < hb2) o16[ga + lane] = (uint16_t)(mine >> (16 * (lane & 1)));
-      const uint16_t* i16 =
-          reinterpret_cast<const uint16_t*>(s_in + tok * R) + 2 * ga;
-      uint16_t* q16 = o16 + ga + hb2;
-      for (int j = lane; j < p2; j += 32) q16[j] = i16[j];
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        bulk_s2g(f.gdst, s_out, (uint32_t)store_bytes);
+        bulk_commit();
+      }
+    } else if (kind == 1) {
+      if (tid == 0) {
+        bulk_s2g(f.gdst, s_in, (uint32_t)f.load_bytes);
+        bulk_commit();
+      }
+      const int nz = f.zero_bytes >> 4;
+      for (int c = tid; c < nz; c += kFpThreads)
+        reinterpret_cast<uint4*>(f.zero_dst)[c] = make_uint4(0, 0, 0, 0);
     }
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      bulk_s2g(gdst, s_out, (uint32_t)len);
-      bulk_commit();
+    // refill this buffer with the item two ahead
+    if (it + 2 < ie) {
+      if (kind == 1 && tid == 0) bulk_wait_read<0>();
+      __syncthreads();
+      if (warp == 0) produce(it + 2, bsel);
     }
   }
   if (tid == 0) bulk_wait<0>();
   if (bad) atomicOr(p.status, KVTC_FLAG_FORMAT);
 }
 
-// ------------------------------------------------------------------ unpack
-__global__ void __launch_bounds__(kFpThreads, 3) fp_unpack_kernel(
-    const __grid_constant__ FpParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* s_in = smem;
-  uint8_t* s_out = smem + kFpInBytes;
-  __shared__ uint64_t bar;
-  __shared__ int abort_flag;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) {
-    mbar_init(&bar, 1);
-    abort_flag = 0;
-    fence_mbar_init();
+// Per-device launch facts, looked up once: SM count, and whether the tile
+// kernels' shared-memory limit has been raised on the device.
+constexpr int kFpMaxDev = 64;
+int g_fp_sms[kFpMaxDev];
+bool g_fp_smem_set[kFpMaxDev][2];
+
+int fp_device() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return dev >= 0 && dev < kFpMaxDev ? dev : 0;
+}
+
+void fp_allow_smem(const void* func) {
+  const int dev = fp_device();
+  const int which = func == (const void*)fp_tile_kernel<true> ? 0 : 1;
+  if (!g_fp_smem_set[dev][which]) {
+    cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         kFpSmem);
+    g_fp_smem_set[dev][which] = true;
   }
-  __syncthreads();
-  uint32_t phase = 0;
-  for (int item = blockIdx.x; item < p.total_items; item += gridDim.x) {
-    const int i = fp_find_stream(p, item);
-    const FpStream& S = p.s[i];
-    const int local = item - S.item_begin;
-    const int ga = S.ga, tb = fp_table_bytes(ga), nslot = 2 * ga;
-    const int64_t off = p.offsets[p.first + i];
-    const int64_t end = p.offsets[p.first + i + 1];
-    // the header is read only once the offsets are known to frame it
-    bool ok = off >= 0 && (off & 15) == 0 && end <= p.in_bytes &&
-              end - off >= kFpHeader + tb;
-    int vmin = 0, d = 0, rp = 0;
-    FpSlots sl = {0, 0, 0, 0};
-    if (ok) {
-      const uint32_t* h = reinterpret_cast<const uint32_t*>(p.in + off);
-      const uint32_t h0 = h[0], h1 = h[1], h2 = h[2];
-      if (lane < nslot) {
-        const uint16_t e =
-            reinterpret_cast<const uint16_t*>(p.in + off + kFpHeader)[lane];
-        vmin = e & 0xff;
-        d = e >> 8;
-      }
-      const bool slot_ok = lane >= nslot || (d <= 6 && vmin <= 63);
-      sl = fp_slots_from(vmin, d, nslot);
-      rp = 2 * ga + 2 * ((sl.hbits + 15) >> 4) + (S.used - 4 * ga);
-      ok = __all_sync(0xffffffffu, slot_ok) && h0 == kFpMagic &&
-           h1 == (uint32_t)S.tc && (h2 & 0xffffu) == (uint32_t)rp &&
-           (h2 >> 16) == (uint32_t)nslot &&
-           end - off == fp_align256(kFpHeader + tb + S.raw_bytes +
-                                    (int64_t)S.tc * rp);
-    }
-    if (!ok) {
-      if (tid == 0) atomicOr(p.status, KVTC_FLAG_FORMAT);
-      continue;
-    }
-    const uint8_t* body = p.in + off + kFpHeader + tb;
-    uint8_t* obase = p.out + S.out_off;
-    const int64_t out_end =
-        S.out_off + fp_align256(S.raw_bytes + (int64_t)S.tc * S.R);
-    if (local < S.nraw) {
-      const int64_t b0 = (int64_t)local * kFpRawChunk;
-      const int64_t b1 = min(S.raw_bytes, b0 + kFpRawChunk);
-      fp_block_copy(obase + b0, body + b0, b1 - b0);
-      if (S.tc == 0 && local == S.nraw - 1)
-        fp_block_zero(obase + S.raw_bytes, out_end - S.out_off - S.raw_bytes);
-      continue;
-    }
-    const int tile = local - S.nraw;
-    const int t0 = tile * kFpTile;
-    const int ntok = min(kFpTile, S.tc - t0);
-    const int R = S.R, R2 = R >> 1, u2 = S.used >> 1;
-    const int hb2 = (sl.hbits + 15) >> 4;
-    uint8_t* gdst = obase + S.raw_bytes + (int64_t)t0 * R;
-    const int len = tile == S.ntiles - 1 ? (int)(p.out + out_end - gdst)
-                                         : ntok * R;
-    if (tid == 0) bulk_wait_read<0>();
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      const uint32_t bytes = (uint32_t)((ntok * rp + 15) & ~15);
-      mbar_arrive_expect_tx(&bar, bytes);
-      bulk_g2s(s_in, body + S.raw_bytes + (int64_t)t0 * rp, bytes, &bar);
-    }
-    for (int b = ntok * R + tid; b < len; b += kFpThreads) s_out[b] = 0;
-    const bool got = mbar_wait(&bar, phase, &abort_flag);
-    phase ^= 1u;
-    if (__syncthreads_or(!got)) {
-      if (tid == 0) {
-        atomicOr(p.status, KVTC_FLAG_TIMEOUT);
-        mbar_drain(&bar, phase ^ 1u);
-      }
-      break;
-    }
-    for (int tok = warp; tok < ntok; tok += kFpWarps) {
-      const uint8_t* ib = s_in + tok * rp;
-      const uint16_t* i16 = reinterpret_cast<const uint16_t*>(ib);
-      uint16_t* o16 = reinterpret_cast<uint16_t*>(s_out + tok * R);
-      if (lane < nslot) {
-        const int k = sl.pos >> 4;
-        const uint32_t bits =
-            (uint32_t)i16[ga + k] | ((uint32_t)i16[ga + k + 1] << 16);
-        const uint32_t code = (bits >> (sl.pos & 15)) & ((4u << sl.d) - 1);
-        const uint32_t u = code & ((1u << sl.d) - 1), m2 = code >> sl.d;
-        const uint32_t hi = (((u + sl.vmin) << 2) | m2) & 0xffu;
-        o16[lane] = (uint16_t)(ib[lane] | (hi << 8));
-      }
-      for (int j = 2 * ga + lane; j < R2; j += 32)
-        o16[j] = j < u2 ? i16[hb2 - ga + j] : (uint16_t)0;
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      bulk_s2g(gdst, s_out, (uint32_t)len);
-      bulk_commit();
-    }
-  }
-  if (tid == 0) bulk_wait<0>();
 }
 
 int fp_blocks(int items) {
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int cap = 3 * (sms > 0 ? sms : 1);
+  const int dev = fp_device();
+  if (g_fp_sms[dev] == 0) {
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    g_fp_sms[dev] = sms > 0 ? sms : 1;
+  }
+  const int cap = 2 * g_fp_sms[dev];
   return items < cap ? (items > 0 ? items : 1) : cap;
 }
 
@@ -527,9 +637,9 @@ cudaError_t launch_fields_pack(const FpParams& p, cudaStream_t st) {
   fp_layout_kernel<<<1, kFpLayoutThreads, 0, st>>>(p);
   count_launch();
   if (p.total_items > 0) {
-    cudaFuncSetAttribute((const void*)fp_pack_kernel,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, kFpSmem);
-    fp_pack_kernel<<<fp_blocks(p.total_items), kFpThreads, kFpSmem, st>>>(p);
+    fp_allow_smem((const void*)fp_tile_kernel<true>);
+    fp_tile_kernel<true>
+        <<<fp_blocks(p.total_items), kFpThreads, kFpSmem, st>>>(p);
     count_launch();
   }
   return cudaGetLastError();
@@ -537,9 +647,9 @@ cudaError_t launch_fields_pack(const FpParams& p, cudaStream_t st) {
 
 cudaError_t launch_fields_unpack(const FpParams& p, cudaStream_t st) {
   if (p.n == 0 || p.total_items == 0) return cudaSuccess;
-  cudaFuncSetAttribute((const void*)fp_unpack_kernel,
-                       cudaFuncAttributeMaxDynamicSharedMemorySize, kFpSmem);
-  fp_unpack_kernel<<<fp_blocks(p.total_items), kFpThreads, kFpSmem, st>>>(p);
+  fp_allow_smem((const void*)fp_tile_kernel<false>);
+  fp_tile_kernel<false>
+      <<<fp_blocks(p.total_items), kFpThreads, kFpSmem, st>>>(p);
   count_launch();
   return cudaGetLastError();
 }

@@ -957,7 +957,8 @@ void fp_fill(FpParams* p, const kvtc_calib* c, const std::vector<int>& cs,
     f.out_off = codec_off[i];
     f.raw_bytes = (s_ + w_) * h.D * 2;
     f.tc = (int32_t)tc;
-    f.ntiles = (int32_t)((tc + kFpTile - 1) / kFpTile);
+    f.tile = (int16_t)((kFpRawChunk / h.R) & ~15);
+    f.ntiles = (int32_t)((tc + f.tile - 1) / f.tile);
     f.nraw = (int32_t)((f.raw_bytes + kFpRawChunk - 1) / kFpRawChunk);
     f.ga = (int16_t)h.Ga;
     f.used = (int16_t)record_used(h);

@@ -153,8 +153,8 @@ struct RawParams {
 constexpr int kFpMaxStream = 256;
 constexpr int kFpChunks = 8;          // min/max partial results per stream
 constexpr int kFpWorkWords = 32;      // u32 words per (stream, chunk)
-constexpr int kFpTile = 128;          // tokens per pack / unpack tile
-constexpr int kFpRawChunk = 32768;    // raw-row bytes per copy item
+constexpr int kFpRawChunk = 32768;    // raw-row bytes per copy item; a
+                                      // record tile is at most this long
 constexpr int kFpHeader = 16;         // packed stream header bytes
 struct FpStream {
   int64_t in_off;       // pack: codec stream offset in the input
@@ -162,12 +162,12 @@ struct FpStream {
   int64_t raw_bytes;    // (s' + w') * D * 2
   int32_t tc;           // compressed tokens
   int32_t item_begin;   // first work item of this stream
-  int32_t ntiles;       // ceil(tc / kFpTile)
+  int32_t ntiles;       // ceil(tc / tile)
   int32_t nraw;         // ceil(raw_bytes / kFpRawChunk)
   int16_t ga;           // active groups
   int16_t used;         // used bytes of a codec record
   int16_t R;            // codec record bytes
-  int16_t pad;
+  int16_t tile;         // tokens per record tile: (kFpRawChunk / R) & ~15
 };
 struct FpParams {
   FpStream s[kFpMaxStream];
