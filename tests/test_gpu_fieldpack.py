@@ -202,3 +202,39 @@ def test_full_llama31_8b_8k_round_trip(kv, torch):
     # the stage saves bytes on this workload
     assert o[-1] < 0.95 * total
     calib.free()
+
+
+def test_more_streams_than_one_launch_group(kv, torch):
+    """300 streams (150 layers x K, V) in one call: the packer runs two
+    launch groups, the second starting from the offset the first wrote."""
+    from oracle import calibrate
+    w = synth.WORKLOADS["tiny"]
+    mu, V, evals, widths, _ = calibrate.calibrate_stream(
+        synth.calib_tokens(w, 0, 0), w.budget_bits)
+    entries = [(l, k, mu, V, evals, widths)
+               for l in range(150) for k in (0, 1)]
+    blob = calibrate.write_blob(entries, w.sink, w.window, w.budget_bits)
+    sc = stream_calibs(blob)[(0, 0)][0]
+    calib = kv.kvtc_calib_load(blob, 0)
+    T = 300
+    order = [(l, k) for l in range(150) for k in (0, 1)]
+    cbs = [codec.compress_stream(synth.eval_tokens(w, l, k, T=T), sc)
+           for l, k in order]
+    pbs = [fieldpack.pack_stream(b, T, sc) for b in cbs]
+    cb, pb = b"".join(cbs), b"".join(pbs)
+    bound = kv.kvtc_fields_bound(calib, 0, 150, 3, T)
+    ws = kv.kvtc_fields_workspace_bytes(calib, 0, 150, 3)
+    dst = torch.full((bound,), 0xA5, dtype=torch.uint8, device="cuda")
+    offs = torch.full((301,), -7, dtype=torch.int64, device="cuda")
+    work = torch.empty(ws, dtype=torch.uint8, device="cuda")
+    kv.kvtc_fields_pack(calib, 0, 150, 3, dev_bytes(torch, cb), len(cb), T,
+                        dst, bound, offs, work, ws)
+    assert kv.kvtc_device_status(calib) == 0
+    want = np.concatenate([[0], np.cumsum([len(p) for p in pbs])])
+    np.testing.assert_array_equal(offs.cpu().numpy(), want)
+    assert dst.cpu().numpy()[:len(pb)].tobytes() == pb
+    out = torch.zeros(len(cb), dtype=torch.uint8, device="cuda")
+    kv.kvtc_fields_unpack(calib, 0, 150, 3, dst, bound, offs, T, out, len(cb))
+    assert kv.kvtc_device_status(calib) == 0
+    assert out.cpu().numpy().tobytes() == cb
+    calib.free()
