@@ -133,8 +133,12 @@ int kvtc_compress(const kvtc_calib* calib, int layer0, int nlayers,
 
 /*
  * kvtc_decompress -- technical summary 2C.
- *   src, src_bytes  : device input written by kvtc_compress (same layers,
- *                     kv_mask and T).
+ *   src, src_bytes  : input written by kvtc_compress (same layers, kv_mask
+ *                     and T), in device memory or in pinned host memory
+ *                     (cudaHostAlloc / cudaHostRegister).  Pinned host
+ *                     memory is read by the kernels themselves over the
+ *                     host link (on GB300, NVLink-C2C), with no staging
+ *                     copy.  Pageable host memory: EINVAL.
  *   dst             : HOST array of 2*nlayers device pointers (as src of
  *                     kvtc_compress), each bf16 [T][ld].
  *   layer_events    : NULL, or a HOST array of nlayers cudaEvent_t (as
@@ -152,8 +156,9 @@ int kvtc_decompress(const kvtc_calib* calib, int layer0, int nlayers,
 /*
  * kvtc_decompress_paged -- restore R requests into a paged KV pool (the
  * block-paged prefix cache of technical summary section 1).
- *   src          : HOST array [R] of device pointers; src[r] holds request
- *                  r's streams as kvtc_compress wrote them.
+ *   src          : HOST array [R] of pointers; src[r] holds request r's
+ *                  streams as kvtc_compress wrote them, in device memory or
+ *                  pinned host memory (as for kvtc_decompress).
  *   T            : HOST array [R] of token counts.
  *   block_table  : DEVICE int32 [R][max_blocks]; token t of request r goes
  *                  to block block_table[r*max_blocks + t/block_size], row

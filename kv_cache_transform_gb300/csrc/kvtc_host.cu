@@ -270,6 +270,27 @@ int pairs_for(int max_pairs, int items) {
   return std::max(1, std::min(items, max_pairs));
 }
 
+// The compressed input of a restore may sit in device memory, or in pinned
+// host memory, which is mapped into the device's address space: the kernels
+// then read it over the host link themselves, with no staging copy.
+// Pageable host memory cannot be read by the kernels and is refused.
+int resolve_input(const void* p, const void** dev) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return KVTC_EINVAL;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+    *dev = p;
+    return KVTC_OK;
+  }
+  if (a.type == cudaMemoryTypeHost && a.devicePointer) {
+    *dev = a.devicePointer;
+    return KVTC_OK;
+  }
+  return KVTC_EINVAL;
+}
+
 }  // namespace
 
 extern "C" {
@@ -721,6 +742,10 @@ int kvtc_decompress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
   DeviceGuard guard(c->device);
   if (!guard.ok) return KVTC_ECUDA;
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  if (need > 0) {
+    st = resolve_input(src, &src);
+    if (st != KVTC_OK) return st;
+  }
   const char* in = static_cast<const char*>(src);
 
   // Launch groups: all streams at once, or one layer at a time when the
@@ -859,6 +884,11 @@ int kvtc_decompress_paged(const kvtc_calib* c, int layer0, int nlayers,
   DeviceGuard guard(c->device);
   if (!guard.ok) return KVTC_ECUDA;
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  std::vector<const void*> in(R);
+  for (int r = 0; r < R; ++r) {
+    st = resolve_input(src[r], &in[r]);
+    if (st != KVTC_OK) return st;
+  }
   PagedParams* p = new (std::nothrow) PagedParams;
   if (!p) return KVTC_ENOMEM;
   const HostStream& h0 = c->hs[cs[0]];
@@ -873,7 +903,7 @@ int kvtc_decompress_paged(const kvtc_calib* c, int layer0, int nlayers,
       int64_t s_, w_, tc;
       split_tokens(T[r], c->sink, c->window, &s_, &w_, &tc);
       const int i = r - r0;
-      p->src[i] = static_cast<const uint8_t*>(src[r]);
+      p->src[i] = static_cast<const uint8_t*>(in[r]);
       p->sbytes[i] = stream_bytes_of(c, h0, T[r]);
       p->tc[i] = (int32_t)tc;
       p->s_[i] = (int32_t)s_;

@@ -257,6 +257,60 @@ def test_layer_events_match_single_launch(kv, torch):
     calib.free()
 
 
+def test_restore_from_pinned_host_memory(kv, torch):
+    """kvtc_decompress and kvtc_decompress_paged given pinned host memory
+    read it over the host link and restore exactly what they restore from
+    device memory; pageable host memory is refused before any launch."""
+    name = "llama31_8b_8k"
+    w = synth.WORKLOADS[name]
+    streams = [(l, k) for l in range(2) for k in (0, 1)]
+    entries = calibrate_workload(name, streams)
+    blob = blob_for(name, entries)
+    calib = kv.kvtc_calib_load(blob, 0)
+    T = 700
+    src = [to_dev(torch, synth.eval_tokens(w, l, k, T=T)) for l, k in streams]
+    total = sum(calib.stream_bytes(l, k, T) for l, k in streams)
+    comp = torch.zeros(total, dtype=torch.uint8, device="cuda")
+    kv.kvtc_compress(calib, 0, 2, 3, src, w.D, T, comp, total)
+    pinned = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    pinned.copy_(comp)
+    torch.cuda.synchronize()
+
+    def restore(inp):
+        out = [torch.full((T, w.D), 0x7FC0, dtype=torch.int16, device="cuda")
+               for _ in streams]
+        kv.kvtc_decompress(calib, 0, 2, 3, inp, total, T, out, w.D)
+        torch.cuda.synchronize()
+        return out
+
+    for x, y in zip(restore(comp), restore(pinned)):
+        assert torch.equal(x, y)
+    assert kv.kvtc_device_status(calib) == 0
+    # paged, one request, from pinned memory
+    bs, maxb = 16, -(-T // 16)
+    bt = torch.arange(maxb, dtype=torch.int32, device="cuda").view(1, maxb)
+    caches = [torch.zeros((maxb, bs, w.D), dtype=torch.int16, device="cuda")
+              for _ in streams]
+    kv.kvtc_decompress_paged(calib, 0, 2, 3, [pinned], [T], bt, maxb, bs,
+                             caches, maxb)
+    torch.cuda.synchronize()
+    ref = restore(comp)
+    for c, r in zip(caches, ref):
+        assert torch.equal(c.view(-1, w.D)[:T], r)
+    assert kv.kvtc_device_status(calib) == 0
+    # pageable host memory: refused on the host
+    pageable = np.zeros(total + 16, dtype=np.uint8)
+    addr = (pageable.ctypes.data + 15) // 16 * 16
+    with pytest.raises(kv.KvtcError) as e:
+        kv.kvtc_decompress(calib, 0, 2, 3, addr, total, T, ref, w.D)
+    assert e.value.code == kv.KVTC_EINVAL
+    with pytest.raises(kv.KvtcError) as e:
+        kv.kvtc_decompress_paged(calib, 0, 2, 3, [addr], [T], bt, maxb, bs,
+                                 caches, maxb)
+    assert e.value.code == kv.KVTC_EINVAL
+    calib.free()
+
+
 def test_full_llama31_8b_8k_sampled(kv, torch):
     """Full workload as the bench launches it (64 streams x 8192 tokens, one
     call each way); eight streams are checked against the oracle in full."""
