@@ -332,6 +332,14 @@ def run_ours(args):
     # soon as layer l is back): one untimed call with an event per layer
     layer_streaming = run_layer_streaming(kv, torch, calib, w, comp, out,
                                           total, stream)
+    # the same with the compressed streams in pinned host memory, read by
+    # the kernels over the host link (restore from host storage)
+    host_comp = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    host_comp.copy_(comp)
+    torch.cuda.synchronize()
+    layer_streaming["from_pinned_host"] = run_layer_streaming(
+        kv, torch, calib, w, host_comp, out, total, stream)
+    del host_comp
 
     # end to end through the public API with host buffers: compressed
     # streams in pinned host memory -> device -> restore; the status word
