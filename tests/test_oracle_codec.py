@@ -201,3 +201,38 @@ def test_all_eight_bits_full_rank_is_accurate(tiny_calib):
     # error norm is at most half a step per coefficient (Parseval)
     bound = np.sqrt(((rng_g / 255 / 2) ** 2 * 16).sum(1))[w.sink:256 - w.window]
     assert np.all(np.sqrt((err ** 2).sum(1)) <= bound * 1.01 + 1e-3)
+
+
+# --------------------------------------------------------------- paged write
+def test_paged_write_identity_table_is_a_reshape():
+    """With block table 0, 1, 2, ... the pool is the rows cut into blocks."""
+    rng = np.random.default_rng(9)
+    T, bs, D = 50, 16, 8
+    rows = rng.integers(0, 2 ** 16, (T, D)).astype(np.uint16)
+    nb = -(-T // bs)
+    pool = np.full((nb, bs, D), 0xFFFF, dtype=np.uint16)
+    codec.paged_write(pool, rows, np.arange(nb), bs)
+    flat = pool.reshape(nb * bs, D)
+    np.testing.assert_array_equal(flat[:T], rows)
+    assert np.all(flat[T:] == 0xFFFF)          # the ragged block's tail
+
+
+def test_paged_write_permuted_table_inverse():
+    """Every pool row holds the token its block and slot name; blocks the
+    table does not name are untouched."""
+    rng = np.random.default_rng(10)
+    T, bs, D = 77, 16, 4
+    rows = np.arange(T * D, dtype=np.uint16).reshape(T, D)
+    nb_used = -(-T // bs)
+    table = rng.permutation(12)[:nb_used]
+    pool = np.full((12, bs, D), 0xFFFF, dtype=np.uint16)
+    codec.paged_write(pool, rows, table, bs)
+    for j, blk in enumerate(table):
+        for slot in range(bs):
+            t = j * bs + slot
+            if t < T:
+                np.testing.assert_array_equal(pool[blk, slot], rows[t])
+            else:
+                assert np.all(pool[blk, slot] == 0xFFFF)
+    for blk in set(range(12)) - set(table.tolist()):
+        assert np.all(pool[blk] == 0xFFFF)
