@@ -79,3 +79,21 @@ def test_bf16_single_rounding_from_fp64():
     q = 2.0 ** -133
     v = np.array([3.4 * q, 2.5 * q, 3.5 * q])
     np.testing.assert_array_equal(fp.bf16_rne_value(v), [3 * q, 2 * q, 4 * q])
+
+
+def test_fp16_bit_views_against_the_format():
+    """fp16_from_bits decodes every finite binary16 pattern to the value the
+    format defines (sign, 5-bit biased exponent, 10-bit fraction, subnormals
+    at 2^-14 * f/1024), and fp16_bits gives the pattern back."""
+    b = np.arange(1 << 16, dtype=np.uint32)
+    sign = np.where(b >> 15, -1.0, 1.0)
+    e = (b >> 10) & 0x1F
+    f = (b & 0x3FF).astype(np.float64)
+    finite = e != 0x1F
+    want = np.where(e == 0, sign * np.ldexp(f / 1024.0, -14),
+                    sign * np.ldexp(1.0 + f / 1024.0, e.astype(np.int64) - 15))
+    got = fp.fp16_from_bits(b.astype(np.uint16)).astype(np.float64)
+    np.testing.assert_array_equal(got[finite], want[finite])
+    back = fp.fp16_bits(fp.fp16_from_bits(b[finite].astype(np.uint16)))
+    np.testing.assert_array_equal(back, b[finite].astype(np.uint16))
+    assert np.all(np.isinf(got[(e == 0x1F) & ((b & 0x3FF) == 0)]))
