@@ -131,3 +131,38 @@ def test_blob_round_trip(tiny):
     bad[40] ^= 1
     with pytest.raises(AssertionError):
         calibrate.read_blob(bytes(bad))
+
+
+@pytest.mark.parametrize("b", range(1, 9))
+def test_distortion_table_equals_codec_error_at_every_width(tiny, b):
+    """Column b of the distortion table is the squared error the codec
+    itself makes at uniform width b (kvtc page, technical summary 2A: the
+    DP minimises reconstruction error measured on calibration data).
+
+    The codec path is independent of the table's own loop: every group is
+    given width b through the stream's widths, the rows are compressed into
+    records (fields and bit-planes), unpacked and reconstructed as
+    x_hat = mu + V c_hat in fp64.  With the full orthonormal basis,
+    Parseval makes ||x - x_hat||^2 equal to ||c - c_hat||^2, so the summed
+    column must match the reconstruction error in x space, and each group's
+    entry the error of its 16 coefficients."""
+    w, cb, (mu, evals, V) = tiny
+    G = w.D // 16
+    x = fp.bf16_bits_to_f64(cb)
+    c = (x - mu) @ V
+    E = calibrate.distortion_table(c)
+    widths = np.full(G, b)
+    budget = G * (32 + 16 * 8)
+    sc = codec.StreamCalib(mu, V, widths, 0, 0, budget)
+    buf = codec.compress_stream(cb, sc)
+    xh = codec.decompress_stream(buf, cb.shape[0], sc, exact=True)
+    err_x = ((x - xh) ** 2).sum()
+    np.testing.assert_allclose(E[:, b].sum(), err_x, rtol=1e-9)
+    shift, scale, q = codec.unpack(codec.stream_records(buf, cb.shape[0], sc),
+                                   sc.bits)
+    chat = codec.dequantise(shift, scale, q)
+    per_group = ((c - chat) ** 2).reshape(len(c), G, 16).sum(axis=(0, 2))
+    np.testing.assert_allclose(E[:, b], per_group, rtol=1e-9, atol=0)
+    # a wider code never does worse on the same group
+    if b > 1:
+        assert np.all(E[:, b] <= E[:, b - 1] * (1 + 1e-12))
