@@ -305,13 +305,18 @@ int kvtc_wait_selftest(const kvtc_calib* calib, uint32_t limit_us,
  *   tokens : device bf16 rows [N][ld] (N >= 1, ld >= D).
  *   mu_out : device fp64 [D], written.
  *   D      : at most 4096; wider rows return KVTC_ESIZE.
- * Scratch comes from a fixed 1 MiB array inside the library, held by every
- * GPU that loads the library until the process exits.  The first call on a
- * device looks up that array's device address (a one-time set-up); make
- * that first call before any stream capture.  All calls share the array:
- * each call writes every entry it reads, but calls that overlap on the GPU
- * race with each other.  No cudaMalloc, cudaFree or allocating library
- * routine is called.  Enqueued on cuda_stream.
+ * Scratch comes from a fixed 1 MiB array inside the library.  CUDA loads
+ * modules lazily by default, so the array comes into being on a device at
+ * the first call there, which loads this code and looks up the array's
+ * device address (a one-time set-up), and it is then held until the process
+ * exits.  That first call can therefore fail with ECUDA when the device has
+ * no free memory left: make it before reserving the device's memory for a
+ * KV pool (or run with CUDA_MODULE_LOADING=EAGER, which creates the array
+ * with the context), and before any stream capture.  All calls on a device
+ * share the array: each call writes every entry it reads, but calls that
+ * overlap on the GPU race with each other, so serialise them.  No
+ * cudaMalloc, cudaFree or allocating library routine is called.  Enqueued
+ * on cuda_stream.
  * Errors: EINVAL, ESIZE, ECUDA.
  */
 int kvtc_calib_mean_static(int cuda_device, const void* tokens, int64_t N,

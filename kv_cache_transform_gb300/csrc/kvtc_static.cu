@@ -18,10 +18,11 @@ namespace {
 constexpr int kStaticMaxD = 4096;   // widest row the scratch array holds
 constexpr int kStaticChunks = 32;   // row chunks summed independently
 
-// Partial column sums [chunk][channel].  Every GPU that loads the library
-// holds this 1 MiB until the process exits.  All calls on a device share
-// it; each call writes every entry it later reads, so nothing needs
-// clearing, but two calls that run at the same time on the GPU race.
+// Partial column sums [chunk][channel].  Modules load lazily, so this
+// 1 MiB comes into being on a device at the first call there and stays
+// until the process exits.  All calls on a device share it; each call
+// writes every entry it later reads, so nothing needs clearing, but two
+// calls that run at the same time on the GPU race.
 static __device__ __align__(256) double g_mean_partial[kStaticChunks *
                                                        kStaticMaxD];
 

@@ -2,10 +2,11 @@
 memory themselves (a serving engine's preallocated KV pool) or cannot afford
 the device-wide synchronisation that cudaMalloc / cudaFree bring.
 
-kvtc_calib_mean_static must give the same per-channel mean as the one
-kvtc_calibrate stores in its blob, call after call, while allocating
-nothing: its scratch is a fixed array inside the library.  This file is
-collected last so that a failure here never hides the other tests."""
+kvtc_calib_mean_static must give the oracle's per-channel calibration mean
+(the mu of the kvtc page's calibration, technical summary 2A), call after
+call, while allocating nothing: its scratch is a fixed array inside the
+library.  This file is collected last so that a failure here never hides
+the other tests."""
 import ctypes
 
 import numpy as np
@@ -25,27 +26,44 @@ def kv():
     return kv
 
 
-def test_static_mean_matches_calibrate_on_consecutive_calls(kv):
+def test_static_mean_matches_oracle_on_consecutive_calls(kv):
     import torch
     cases = [("tiny", 0, 0), ("llama31_8b_8k", 5, 1)]
-    rows, refs = [], []
+    rows, refs, outs = [], [], []
     for name, layer, k in cases:
         w = synth.WORKLOADS[name]
         r = synth.calib_tokens(w, layer, k)
-        d = torch.from_numpy(r.view(np.int16).copy()).cuda()
-        blob = kv.kvtc_calibrate([d], [layer], [k], w.n_calib, w.D, w.D,
-                                 w.sink, w.window, w.budget_bits)
-        refs.append(calibrate.read_blob(blob)["streams"][0]["mu"])
-        rows.append((d, w))
+        refs.append(calibrate.pca(r)[0])       # the oracle's mean
+        rows.append((torch.from_numpy(r.view(np.int16).copy()).cuda(), w))
+        outs.append(torch.empty(w.D, dtype=torch.float64, device="cuda"))
     # two calls in a row on different inputs, then the first one again: the
     # shared scratch must not carry anything from one call to the next
     for i in (0, 1, 0):
         d, w = rows[i]
-        out = torch.full((w.D,), float("nan"), dtype=torch.float64,
-                         device="cuda")
-        kv.kvtc_calib_mean_static(d, w.n_calib, w.D, w.D, out)
-        np.testing.assert_allclose(out.cpu().numpy(), refs[i], rtol=0,
+        outs[i].fill_(float("nan"))
+        kv.kvtc_calib_mean_static(d, w.n_calib, w.D, w.D, outs[i])
+        np.testing.assert_allclose(outs[i].cpu().numpy(), refs[i], rtol=0,
                                    atol=1e-12)
+
+
+def test_static_mean_allocates_no_device_memory(kv):
+    """After the first call on the device (its one-time set-up), further
+    calls leave the driver's free device memory unchanged."""
+    import torch
+    w = synth.WORKLOADS["llama31_8b_8k"]
+    r = synth.calib_tokens(w, 3, 0)
+    d = torch.from_numpy(r.view(np.int16).copy()).cuda()
+    out = torch.empty(w.D, dtype=torch.float64, device="cuda")
+    kv.kvtc_calib_mean_static(d, w.n_calib, w.D, w.D, out)   # set-up
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        kv.kvtc_calib_mean_static(d, w.n_calib, w.D, w.D, out)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    np.testing.assert_allclose(out.cpu().numpy(), calibrate.pca(r)[0],
+                               rtol=0, atol=1e-12)
 
 
 def test_static_mean_rejects_rows_wider_than_its_scratch(kv):
