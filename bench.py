@@ -9,8 +9,13 @@ before the timed region, with the library's own GPU calibration.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-N > 1 runs under torchrun, one rank per GPU, each restoring its own copy
-of the workload (weak scaling; the streams are independent, no collective).
+N > 1 runs under torchrun, one rank per GPU.  The workload's layers are
+split into N contiguous blocks, as a pipeline-parallel deployment holds
+them (kvtc page, technical summary section 4: the 70B model served with
+pipeline parallelism), and rank r compresses and restores only its block.
+The streams are independent, so there is no collective on the data path;
+the job's value is the whole workload's bytes over the slowest rank's time
+(total work fixed as N grows: strong scaling).
 """
 from __future__ import annotations
 
@@ -35,11 +40,44 @@ METRIC = ("restored-KV GB/s (decompress) & compress GB/s at 1 GB300; "
 WORKLOAD = "llama31_8b_8k"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
                   "bf16_tflops_sustained": 1700.0}
-# DRAM bytes per launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum)
-# of the kernel as it is now, per launch of the bench workload (a one-pass
-# capture of the full workload: profiles/launches_llama31_8b_8k.md); None
-# when the kernel has changed since the capture.
-NCU_TRAFFIC = {"decompress": 1125680640, "compress": 1180995584}
+# DRAM bytes per launch measured by ncu live in a committed text file next
+# to the other profile summaries, together with a digest of the kernel
+# sources they were measured on; a digest that no longer matches the
+# sources means the kernels changed since, and the traffic is reported as
+# null.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+KERNEL_SOURCES = ("kvtc_kernels.cu", "kvtc_internal.cuh", "ptx.cuh")
+
+
+def kernel_digest() -> str:
+    """sha256 over the tensor-core kernels' source files."""
+    import hashlib
+    h = hashlib.sha256()
+    base = os.path.join(ROOT, "kv_cache_transform_gb300", "csrc")
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(base, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def read_traffic(workload: str):
+    """{kernel: DRAM bytes per launch} for `workload` from the traffic file,
+    or ({}, reason) when it is absent or was measured on other sources."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return {}, "no capture"
+    digest, out = None, {}
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            parts = line.split()
+            if not parts or line.startswith("#"):
+                continue
+            if parts[0] == "kernel_sources_sha256:" and len(parts) > 1:
+                digest = parts[1]
+            elif len(parts) == 3 and parts[0] == workload:
+                out[parts[1]] = int(parts[2])
+    if digest != kernel_digest():
+        return {}, "kernels changed since the capture"
+    return out, "ncu capture of the current kernels"
 
 
 def load_peaks():
@@ -139,11 +177,20 @@ def max_over_ranks(values, world: int, device="cpu"):
     return [float(v) for v in t.tolist()]
 
 
-def whole_job_gbs(world: int, bytes_per_rank: int, steps: int,
-                  seconds: float) -> float:
-    """Weak scaling: every rank processes its own full copy of the workload,
-    so the job moves world x bytes_per_rank per step."""
-    return world * bytes_per_rank * steps / seconds / 1e9
+def layer_shard(layers: int, world: int, rank: int):
+    """Rank `rank`'s contiguous block of layers: (first layer, count).  The
+    blocks of ranks 0 .. world-1 cover [0, layers) exactly once, in order,
+    their sizes differing by at most one."""
+    if world < 1 or not 0 <= rank < world or layers < world:
+        raise ValueError(f"cannot split {layers} layers over {world} ranks")
+    base, extra = divmod(layers, world)
+    return rank * base + min(rank, extra), base + (1 if rank < extra else 0)
+
+
+def job_gbs(job_bytes: int, steps: int, seconds: float) -> float:
+    """Whole-job throughput: the bytes of every rank's shard (the whole
+    workload) per step, over the slowest rank's time."""
+    return job_bytes * steps / seconds / 1e9
 
 
 # --------------------------------------------------------------- oracle arm
@@ -206,11 +253,12 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ our arm
-def run_ours(args):
+def setup_rank(args):
+    """torch.distributed (NCCL, one rank per GPU) when N > 1; the library
+    built by rank 0 and loaded everywhere; this rank's layer block."""
     import torch
     import kv_cache_transform_gb300 as kv
     from kv_cache_transform_gb300 import _build
-
     rank, world, local = dist_env()
     if world > 1:
         import torch.distributed as dist
@@ -218,29 +266,38 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     else:
         torch.cuda.set_device(0)
-    dev = torch.cuda.current_device()
     if rank == 0:
         _build.build()
     if world > 1:
-        dist.barrier()
+        torch.distributed.barrier()
     kv.lib()
     w = synth.WORKLOADS[args.workload]
     if args.layers:
         import dataclasses
         w = dataclasses.replace(w, layers=min(args.layers, w.layers))
-    streams = w.streams()
-    T, D = w.tokens, w.D
-    stream = torch.cuda.current_stream()
+    layer0, nl = layer_shard(w.layers, world, rank)
+    return torch, kv, rank, world, w, layer0, nl
 
-    # one-time calibration on the GPU (not timed)
+
+def calibrate_shard(kv, torch, w, streams, dev):
+    """One-time GPU calibration of this rank's streams (not timed)."""
     t0 = time.perf_counter()
     cal = [synth.calib_tokens_torch(w, l, k) for l, k in streams]
     blob = kv.kvtc_calibrate(cal, [l for l, _ in streams],
-                             [k for _, k in streams], w.n_calib, D, D,
+                             [k for _, k in streams], w.n_calib, w.D, w.D,
                              w.sink, w.window, w.budget_bits, device=dev)
     del cal
     calib = kv.kvtc_calib_load(blob, dev)
-    calib_s = time.perf_counter() - t0
+    return calib, time.perf_counter() - t0
+
+
+def run_ours(args):
+    torch, kv, rank, world, w, layer0, nl = setup_rank(args)
+    dev = torch.cuda.current_device()
+    streams = [(l, k) for l in range(layer0, layer0 + nl) for k in w.kv]
+    T, D = w.tokens, w.D
+    stream = torch.cuda.current_stream()
+    calib, calib_s = calibrate_shard(kv, torch, w, streams, dev)
     ks = sorted({calib.query(l, k)["k"] for l, k in streams})
 
     x = [synth.eval_tokens_torch(w, l, k, T=T) for l, k in streams]
@@ -250,10 +307,10 @@ def run_ours(args):
            for _ in streams]
 
     def compress():
-        kv.kvtc_compress(calib, 0, w.layers, 3, x, D, T, comp, total, stream)
+        kv.kvtc_compress(calib, layer0, nl, 3, x, D, T, comp, total, stream)
 
     def decompress():
-        kv.kvtc_decompress(calib, 0, w.layers, 3, comp, total, T, out, D,
+        kv.kvtc_decompress(calib, layer0, nl, 3, comp, total, T, out, D,
                            stream)
 
     for _ in range(max(3, args.warmup)):
@@ -269,7 +326,7 @@ def run_ours(args):
     launches0 = kv.kvtc_launch_count()
     with ClockSampler(dev) as clocks:
         if world > 1:
-            dist.barrier()
+            torch.distributed.barrier()
         torch.cuda.synchronize()
         for i in range(args.steps):
             ev[i][0].record(stream)
@@ -279,8 +336,9 @@ def run_ours(args):
             ev[i][2].record(stream)
         torch.cuda.synchronize()
         if world > 1:
-            dist.barrier()
-    launches = kv.kvtc_launch_count() - launches0
+            torch.distributed.barrier()
+        launches = kv.kvtc_launch_count() - launches0
+        extra = extend_clock_window(clocks, [compress, decompress], torch)
     t_comp = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
     t_dec = sum(e[1].elapsed_time(e[2]) for e in ev) / 1e3
     med_comp = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
@@ -290,7 +348,7 @@ def run_ours(args):
                                            device="cuda")
     flags = kv.kvtc_device_status(calib)
 
-    # algorithmic bytes and FLOPs of one pass (per direction)
+    # algorithmic bytes and FLOPs of one pass of this rank (per direction)
     s_ = min(w.sink, T)
     w_ = min(w.window, T - s_)
     tc = T - s_ - w_
@@ -300,11 +358,15 @@ def run_ours(args):
     dec_bytes = rec + raw_rows + raw_kv          # records + raw in, all out
     comp_bytes = raw_kv + rec + raw_rows         # all in, records + raw out
     flops = sum(2 * D * calib.query(l, k)["k"] * tc for l, k in streams)
+    job_raw = w.raw_bytes()                      # every rank's shard
+    job_rec = job_raw * (rec + raw_rows) // raw_kv
     peaks, peak_kind = load_peaks()
     hbm = float(peaks["hbm_gbs"])
     tflops = float(peaks["bf16_tflops"])
+    traffic, traffic_src = read_traffic(w.name) if world == 1 and \
+        nl == synth.WORKLOADS[w.name].layers else ({}, "other workload")
 
-    def roof(nbytes, t, name):
+    def roof(nbytes, t, name, kernel):
         t_mem = nbytes / (hbm * 1e9)
         t_mma = flops / (tflops * 1e12)
         per = t / args.steps
@@ -316,63 +378,71 @@ def run_ours(args):
             ach = flops / per / 1e12
             r = {"bound": "tensor", "achieved": ach, "peak": tflops,
                  "unit": "TFLOP/s", "frac": ach / tflops}
-        r.update({"traffic": NCU_TRAFFIC[name], "kernel": name,
+        r.update({"traffic": traffic.get(kernel), "traffic_source":
+                  traffic_src, "kernel": name,
                   "algorithmic_bytes": nbytes, "flops": flops,
                   "t_roof_us": 1e6 * max(t_mem, t_mma),
-                  "frac_of_roofline": 1e6 * max(t_mem, t_mma) / (1e6 * per),
+                  "frac_of_roofline": max(t_mem, t_mma) / per,
                   "peak_source": f"{peak_kind} (MEASURED_PEAKS.json burst)"
                   if peak_kind == "measured" else "fallback"})
         return r
 
-    roof_dec = roof(dec_bytes, t_dec, "decompress")
-    roof_comp = roof(comp_bytes, t_comp, "compress")
+    roof_dec = roof(dec_bytes, t_dec, "decompress", "decompress_kernel")
+    roof_comp = roof(comp_bytes, t_comp, "compress", "compress_kernel")
     dominant = roof_dec if t_dec >= t_comp else roof_comp
 
     # layer-wise restore (the TTFT use: attention of layer l can start as
     # soon as layer l is back): one untimed call with an event per layer
-    layer_streaming = run_layer_streaming(kv, torch, calib, w, comp, out,
-                                          total, stream)
+    layer_streaming = run_layer_streaming(kv, torch, calib, w, layer0, nl,
+                                          comp, out, total, stream)
     # the same with the compressed streams in pinned host memory, read by
     # the kernels over the host link (restore from host storage)
     host_comp = torch.empty(total, dtype=torch.uint8, pin_memory=True)
     host_comp.copy_(comp)
     torch.cuda.synchronize()
     layer_streaming["from_pinned_host"] = run_layer_streaming(
-        kv, torch, calib, w, host_comp, out, total, stream)
+        kv, torch, calib, w, layer0, nl, host_comp, out, total, stream)
     del host_comp
+    layer_streaming["overlap"] = run_overlap(kv, torch, calib, w, layer0, nl,
+                                             comp, out, total, stream)
 
-    # end to end through the public API with host buffers: compressed
-    # streams in pinned host memory -> device -> restore; the status word
-    # (the step's result flag) read back; and the compress direction with
-    # raw KV from pinned host memory and the streams read back.
-    e2e = run_e2e(kv, torch, calib, w, comp, out, x, total, stream,
-                  max(3, args.steps // 2))
-    field_packing = run_fieldpack(kv, torch, calib, w, comp, out, total,
-                                  stream, max(3, args.steps // 4))
+    # end to end through the public API with host buffers
+    e2e = run_e2e(kv, torch, calib, w, layer0, nl, comp, out, x, total,
+                  stream, max(3, args.steps // 2))
+    (t_e2e,) = max_over_ranks([e2e.pop("_seconds")], world, device="cuda")
+    e2e["value"] = job_gbs(job_raw, e2e.pop("_steps"), t_e2e)
+    field_packing = run_fieldpack(kv, torch, calib, w, layer0, nl, comp, out,
+                                  total, stream, max(3, args.steps // 4))
 
     line = {
         "metric": METRIC,
-        "value": whole_job_gbs(world, raw_kv, args.steps, t_dec),
+        "value": job_gbs(job_raw, args.steps, t_dec),
         "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * t_step / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_desc(w), "streams": len(streams),
+        "config": {"workload": workload_desc(w), "streams": len(w.streams()),
                    "tokens": T, "D": D, "k": ks,
-                   "record_bytes": calib.query(0, 0)["record_bytes"],
-                   "l2": "inputs larger than L2: 1.07 GB per direction",
-                   "calibration_s": round(calib_s, 2)},
-        "compress": {"value": whole_job_gbs(world, raw_kv, args.steps, t_comp),
+                   "record_bytes": calib.query(layer0, w.kv[0])[
+                       "record_bytes"],
+                   "shard": {"by": "layers", "ranks": world,
+                             "layers_of_rank0": [layer0, layer0 + nl]},
+                   "l2": f"inputs larger than L2: "
+                         f"{raw_kv / 1e9:.2f} GB per direction per rank",
+                   "calibration_s": round(calib_s, 2),
+                   "calibration_s_per_stream": round(calib_s / len(streams),
+                                                     4)},
+        "compress": {"value": job_gbs(job_raw, args.steps, t_comp),
                      "unit": "GB/s", "ms": 1e3 * t_comp / args.steps,
                      "ms_median": med_comp,
-                     "compressed_out_gbs": world * (rec + raw_rows) *
-                     args.steps / t_comp / 1e9},
-        "decompress": {"value": whole_job_gbs(world, raw_kv, args.steps, t_dec),
+                     "compressed_out_gbs": job_gbs(job_rec, args.steps,
+                                                   t_comp)},
+        "decompress": {"value": job_gbs(job_raw, args.steps, t_dec),
                        "unit": "GB/s", "ms": 1e3 * t_dec / args.steps,
                        "ms_median": med_dec,
-                       "compressed_in_gbs": world * (rec + raw_rows) *
-                       args.steps / t_dec / 1e9},
+                       "compressed_in_gbs": job_gbs(job_rec, args.steps,
+                                                    t_dec)},
         "compression_ratio": raw_kv / total,
         "roofline": dominant,
         "rooflines": {"decompress": roof_dec, "compress": roof_comp},
@@ -380,7 +450,7 @@ def run_ours(args):
         "layer_streaming": layer_streaming,
         "field_packing": field_packing,
         "gpu_launches": launches,
-        "clocks": clocks.summary(),
+        "clocks": dict(clocks.summary(), window=extra),
         "device_flags": flags,
     }
     if rank == 0:
@@ -390,57 +460,52 @@ def run_ours(args):
                 "value": nb / dt / 1e9, "unit": "GB/s", "cores": cores,
                 "kind": "oracle",
                 "sample": f"oracle compress + decompress of 1 of "
-                          f"{len(streams)} streams ({T} tokens x D={D}); "
-                          f"restored bytes per second"}
+                          f"{len(w.streams())} streams ({T} tokens x D={D});"
+                          f" restored bytes per second"}
         print(json.dumps(line), flush=True)
     calib.free()
     if world > 1:
-        dist.destroy_process_group()
+        torch.distributed.destroy_process_group()
+
+
+def extend_clock_window(clocks, step_fns, torch, seconds: float = 1.0,
+                        min_samples: int = 40) -> str:
+    """Keep the GPU busy with the same steps (untimed) right after the timed
+    region until the clock sampler has seen enough samples, so that the
+    reported clocks rest on more than the few samples a short timed region
+    allows.  Returns a description of the window."""
+    t0 = time.perf_counter()
+    n = 0
+    while (time.perf_counter() - t0 < seconds and
+           len(clocks.lines) < min_samples):
+        for _ in range(20):
+            for f in step_fns:
+                f()
+        torch.cuda.synchronize()
+        n += 20
+    return (f"timed region plus {n} more steps of the same work "
+            f"({time.perf_counter() - t0:.2f} s)")
 
 
 def run_paged(args):
     """Paged restore: every request's streams compressed once (untimed), then
     kvtc_decompress_paged of all requests into 16-token blocks through the
-    seeded block table, timed.  The paged workload is decompress-only."""
-    import torch
-    import kv_cache_transform_gb300 as kv
-    from kv_cache_transform_gb300 import _build
-
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(0)
+    seeded block table, timed.  The paged workload is decompress-only.
+    Under N ranks each rank restores its block of layers of every
+    request."""
+    torch, kv, rank, world, w, layer0, nl = setup_rank(args)
     dev = torch.cuda.current_device()
-    if rank == 0:
-        _build.build()
-    if world > 1:
-        dist.barrier()
-    kv.lib()
-    w = synth.WORKLOADS[args.workload]
-    if args.layers:
-        import dataclasses
-        w = dataclasses.replace(w, layers=min(args.layers, w.layers))
-    streams = w.streams()
+    streams = [(l, k) for l in range(layer0, layer0 + nl) for k in w.kv]
     T, D, bs = w.tokens, w.D, w.block_size
     stream = torch.cuda.current_stream()
-    t0 = time.perf_counter()
-    cal = [synth.calib_tokens_torch(w, l, k) for l, k in streams]
-    blob = kv.kvtc_calibrate(cal, [l for l, _ in streams],
-                             [k for _, k in streams], w.n_calib, D, D,
-                             w.sink, w.window, w.budget_bits, device=dev)
-    del cal
-    calib = kv.kvtc_calib_load(blob, dev)
-    calib_s = time.perf_counter() - t0
+    calib, calib_s = calibrate_shard(kv, torch, w, streams, dev)
     total = sum(calib.stream_bytes(l, k, T) for l, k in streams)
     srcs = []
     for r in range(w.requests):
         x = [synth.eval_tokens_torch(w, l, k, request=r, T=T)
              for l, k in streams]
         comp = torch.empty(total, dtype=torch.uint8, device="cuda")
-        kv.kvtc_compress(calib, 0, w.layers, 3, x, D, T, comp, total, stream)
+        kv.kvtc_compress(calib, layer0, nl, 3, x, D, T, comp, total, stream)
         srcs.append(comp)
         del x
     table = synth.block_table(w)
@@ -451,7 +516,7 @@ def run_paged(args):
     Ts = [T] * w.requests
 
     def restore(src):
-        kv.kvtc_decompress_paged(calib, 0, w.layers, 3, src, Ts, bt,
+        kv.kvtc_decompress_paged(calib, layer0, nl, 3, src, Ts, bt,
                                  table.shape[1], bs, caches, nblocks, stream)
 
     for _ in range(max(3, args.warmup)):
@@ -464,7 +529,7 @@ def run_paged(args):
     launches0 = kv.kvtc_launch_count()
     with ClockSampler(dev) as clocks:
         if world > 1:
-            dist.barrier()
+            torch.distributed.barrier()
         torch.cuda.synchronize()
         for i in range(args.steps):
             ev[i][0].record(stream)
@@ -472,8 +537,9 @@ def run_paged(args):
             ev[i][1].record(stream)
         torch.cuda.synchronize()
         if world > 1:
-            dist.barrier()
-    launches = kv.kvtc_launch_count() - launches0
+            torch.distributed.barrier()
+        launches = kv.kvtc_launch_count() - launches0
+        extra = extend_clock_window(clocks, [lambda: restore(srcs)], torch)
     t_dec = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
     (t_dec,) = max_over_ranks([t_dec], world, device="cuda")
     flags = kv.kvtc_device_status(calib)
@@ -487,70 +553,83 @@ def run_paged(args):
     dec_bytes = rec + raw_rows + raw_kv
     flops = w.requests * sum(2 * D * calib.query(l, k)["k"] * tc
                              for l, k in streams)
+    job_raw = w.raw_bytes()
     peaks, peak_kind = load_peaks()
     hbm = float(peaks["hbm_gbs"])
     per = t_dec / args.steps
     t_mem = dec_bytes / (hbm * 1e9)
+    traffic, traffic_src = read_traffic(w.name) if world == 1 and \
+        nl == synth.WORKLOADS[w.name].layers else ({}, "other workload")
     roof = {"bound": "hbm", "achieved": dec_bytes / per / 1e9, "peak": hbm,
             "unit": "GB/s", "frac": dec_bytes / per / 1e9 / hbm,
-            "traffic": None, "kernel": "decompress_paged",
+            "traffic": traffic.get("decompress_kernel_paged"),
+            "traffic_source": traffic_src, "kernel": "decompress_paged",
             "algorithmic_bytes": dec_bytes, "flops": flops,
             "t_roof_us": 1e6 * max(t_mem, flops / (float(peaks["bf16_tflops"])
                                                    * 1e12)),
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json burst)"}
-    # end to end: every request's compressed streams H2D from pinned host
-    # memory, the paged restore, the status word read back
+    # end to end: every request's compressed streams in pinned host memory,
+    # read by the kernels over the host link (zero copy), the status word
+    # read back
     host = [torch.empty(total, dtype=torch.uint8, pin_memory=True)
             for _ in srcs]
     for h, d in zip(host, srcs):
         h.copy_(d)
     torch.cuda.synchronize()
     e2e_steps = max(2, min(args.steps, 5))
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    t_e2e = 0.0
     for _ in range(e2e_steps):
-        for h, d in zip(host, srcs):
-            d.copy_(h, non_blocking=True)
-        restore(srcs)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        flush.zero_()
+        a.record(stream)
+        restore(host)
         kv.kvtc_device_status(calib, stream)
-    b.record(stream)
-    torch.cuda.synchronize()
-    t_e2e = a.elapsed_time(b) / 1e3
+        b.record(stream)
+        torch.cuda.synchronize()
+        t_e2e += a.elapsed_time(b) / 1e3
+    (t_e2e,) = max_over_ranks([t_e2e], world, device="cuda")
     line = {
         "metric": METRIC,
-        "value": whole_job_gbs(world, raw_kv, args.steps, t_dec),
+        "value": job_gbs(job_raw, args.steps, t_dec),
         "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * per,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(w) +
                    f", {w.requests} requests, paged blocks of {bs}",
-                   "streams_per_request": len(streams), "tokens": T, "D": D,
+                   "streams_per_request": len(w.streams()), "tokens": T,
+                   "D": D,
                    "k": sorted({calib.query(l, k)["k"] for l, k in streams}),
-                   "record_bytes": calib.query(0, 0)["record_bytes"],
+                   "record_bytes": calib.query(layer0, w.kv[0])[
+                       "record_bytes"],
+                   "shard": {"by": "layers", "ranks": world,
+                             "layers_of_rank0": [layer0, layer0 + nl]},
                    "l2": f"inputs larger than L2: {raw_kv / 1e9:.1f} GB out",
-                   "calibration_s": round(calib_s, 2)},
-        "decompress": {"value": whole_job_gbs(world, raw_kv, args.steps,
-                                              t_dec),
+                   "calibration_s": round(calib_s, 2),
+                   "calibration_s_per_stream": round(calib_s / len(streams),
+                                                     4)},
+        "decompress": {"value": job_gbs(job_raw, args.steps, t_dec),
                        "unit": "GB/s", "ms": 1e3 * per},
         "roofline": roof,
-        "e2e": {"value": raw_kv * e2e_steps / t_e2e / 1e9, "unit": "GB/s",
+        "e2e": {"value": job_gbs(job_raw, e2e_steps, t_e2e), "unit": "GB/s",
+                "mode": "zero copy",
                 "h2d_bytes_per_step": total * len(srcs),
                 "d2h_bytes_per_step": 4},
         "gpu_launches": launches,
-        "clocks": clocks.summary(),
+        "clocks": dict(clocks.summary(), window=extra),
         "device_flags": flags,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
     calib.free()
     if world > 1:
-        dist.destroy_process_group()
+        torch.distributed.destroy_process_group()
 
 
-def run_layer_streaming(kv, torch, calib, w, comp, out, total, stream,
-                        reps: int = 5):
+def run_layer_streaming(kv, torch, calib, w, layer0, nl, comp, out, total,
+                        stream, reps: int = 5):
     """Restore layer by layer (one launch per layer, an event after each)
     and report when the first layer and all layers are back, relative to the
     start of the call: the per-layer restore latency that bounds how early
@@ -559,14 +638,14 @@ def run_layer_streaming(kv, torch, calib, w, comp, out, total, stream,
     first, total_t, per = [], [], []
     for _ in range(reps):
         start = torch.cuda.Event(enable_timing=True)
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(w.layers)]
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(nl)]
         start.record(stream)
         for e in evs:  # torch creates the CUDA event on its first record
             e.record(stream)
         # every launch enqueued behind a sleep: device-side latencies
         torch.cuda._sleep(40_000_000)
         start.record(stream)
-        kv.kvtc_decompress(calib, 0, w.layers, 3, comp, total, T, out, D,
+        kv.kvtc_decompress(calib, layer0, nl, 3, comp, total, T, out, D,
                            stream, layer_events=evs)
         torch.cuda.synchronize()
         ts = [start.elapsed_time(e) * 1e3 for e in evs]
@@ -574,44 +653,151 @@ def run_layer_streaming(kv, torch, calib, w, comp, out, total, stream,
         total_t.append(ts[-1])
         per.append(float(np.median(np.diff([0.0] + ts))))
     return {"timing": "device (launches enqueued before the first starts)",
-            "layers": w.layers, "first_layer_us": float(np.median(first)),
+            "layers": nl, "first_layer_us": float(np.median(first)),
             "all_layers_us": float(np.median(total_t)),
             "median_layer_us": float(np.median(per)),
             "restored_bytes_per_layer": len(w.kv) * T * D * 2}
 
 
-def run_e2e(kv, torch, calib, w, comp, out, x, total, stream, steps):
+def attention_stand_in(torch, k, v, q):
+    """Stand-in for what a model does with a restored layer: the first
+    decode step's attention of one query per KV head over all T restored
+    tokens, softmax(q K^T / sqrt(d)) V.  k, v: bf16 [T][H*d]; q: bf16
+    [H][d]; returns fp32 [H][d]."""
+    H, d = q.shape
+    T = k.shape[0]
+    kh = k.view(T, H, d).transpose(0, 1)            # [H][T][d]
+    vh = v.view(T, H, d).transpose(0, 1)
+    s = torch.bmm(kh, q[:, :, None]).float() / d ** 0.5   # [H][T][1]
+    p = torch.softmax(s, dim=1).to(torch.bfloat16)
+    return torch.bmm(p.transpose(1, 2), vh).float()[:, 0, :]
+
+
+def overlap_schedule(kv, torch, calib, w, layer0, nl, comp, out, total,
+                     stream, q, overlapped: bool):
+    """Restore layers [layer0, layer0 + nl) and run the attention stand-in
+    on each.  Overlapped: the consumer runs on a second stream and waits
+    only for layer l's event, so it works on layer l while later layers are
+    still being restored.  Serial: restore everything, then consume.
+    Everything is enqueued behind a sleep so the events time the device.
+    Returns (per-layer results, ms to the first consumed layer, ms to the
+    last)."""
+    T, D = w.tokens, w.D
+    nk = len(w.kv)
+    assert nk == 2, "the stand-in attends over K and V"
+    start = torch.cuda.Event(enable_timing=True)
+    done = [torch.cuda.Event(enable_timing=True) for _ in range(nl)]
+    evs = [torch.cuda.Event() for _ in range(nl)]
+    cons = torch.cuda.Stream() if overlapped else stream
+    for e in evs + done + [start]:
+        e.record(stream)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(40_000_000)
+    start.record(stream)
+    res = [None] * nl
+    if overlapped:
+        cons.wait_event(start)
+        kv.kvtc_decompress(calib, layer0, nl, 3, comp, total, T, out, D,
+                           stream, layer_events=evs)
+        with torch.cuda.stream(cons):
+            for l in range(nl):
+                cons.wait_event(evs[l])
+                res[l] = attention_stand_in(torch, out[nk * l],
+                                            out[nk * l + 1], q)
+                done[l].record(cons)
+    else:
+        kv.kvtc_decompress(calib, layer0, nl, 3, comp, total, T, out, D,
+                           stream)
+        for l in range(nl):
+            res[l] = attention_stand_in(torch, out[nk * l], out[nk * l + 1],
+                                        q)
+            done[l].record(stream)
+    torch.cuda.synchronize()
+    return res, start.elapsed_time(done[0]), start.elapsed_time(done[-1])
+
+
+def run_overlap(kv, torch, calib, w, layer0, nl, comp, out, total, stream,
+                reps: int = 5):
+    """Restore/consume overlap (layer-wise decompression so generation can
+    start before every layer is back: kvtc page, technical summary 2C and
+    the TTFT results of section 4): time to the first consumed layer and to
+    the last, overlapped against restore-then-consume."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(77)
+    q = torch.randn((w.heads, w.head_dim), generator=g, device="cuda").to(
+        torch.bfloat16)
+    ov, se = [], []
+    for _ in range(reps):
+        _, f, l = overlap_schedule(kv, torch, calib, w, layer0, nl, comp, out,
+                                   total, stream, q, True)
+        ov.append((f, l))
+        _, f, l = overlap_schedule(kv, torch, calib, w, layer0, nl, comp, out,
+                                   total, stream, q, False)
+        se.append((f, l))
+    med = lambda v, i: float(np.median([x[i] for x in v])) * 1e3
+    return {"consumer": "per layer, one query per KV head attending over "
+                        "the T restored tokens (softmax(q K^T / sqrt d) V)",
+            "timing": "device (launches enqueued before the first starts)",
+            "overlapped_first_consumed_us": med(ov, 0),
+            "overlapped_all_consumed_us": med(ov, 1),
+            "serial_first_consumed_us": med(se, 0),
+            "serial_all_consumed_us": med(se, 1)}
+
+
+def run_e2e(kv, torch, calib, w, layer0, nl, comp, out, x, total, stream,
+            steps):
+    """End to end through the public API with host buffers.  The headline
+    mode, fixed in advance, is zero copy: the compressed streams sit in
+    pinned host memory and kvtc_decompress is handed that buffer, so the
+    kernels read it over the host link while they reconstruct; L2 is
+    flushed before each step and the status word is read back after it.
+    Two copy-based modes and the compress direction are reported beside
+    it."""
     T, D = w.tokens, w.D
     host_comp = torch.empty(total, dtype=torch.uint8, pin_memory=True)
     host_comp.copy_(comp)
     dev_comp = torch.empty_like(comp)
-    flags = torch.empty(1, dtype=torch.int32, pin_memory=True)
     raw_kv = len(x) * T * D * 2
     torch.cuda.synchronize()
-    # decompress direction, serial: copy everything, then restore
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
+    # zero copy (the headline mode)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    zc = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+          for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        zc[i][0].record(stream)
+        kv.kvtc_decompress(calib, layer0, nl, 3, host_comp, total, T, out, D,
+                           stream)
+        kv.kvtc_device_status(calib, stream)  # syncs, reads the flags back
+        zc[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_zc = sum(e[0].elapsed_time(e[1]) for e in zc) / 1e3
+    del flush
+    # serial: copy everything, then restore
     a.record(stream)
     for _ in range(steps):
         dev_comp.copy_(host_comp, non_blocking=True)
-        kv.kvtc_decompress(calib, 0, w.layers, 3, dev_comp, total, T, out, D,
+        kv.kvtc_decompress(calib, layer0, nl, 3, dev_comp, total, T, out, D,
                            stream)
-        kv.kvtc_device_status(calib, stream)  # syncs, reads the flags back
+        kv.kvtc_device_status(calib, stream)
     b.record(stream)
     torch.cuda.synchronize()
     t_serial = a.elapsed_time(b) / 1e3
-    # decompress direction, pipelined: the streams of a group of layers are
-    # contiguous in the compressed buffer, so group g + 1 is copied on a
-    # second stream while group g is restored
-    ngroups = 4 if w.layers % 4 == 0 else 1
-    per = w.layers // ngroups
-    sizes = [sum(calib.stream_bytes(l, k, T) for k in w.kv)
-             for l in range(w.layers)]
+    # pipelined: the streams of a group of layers are contiguous in the
+    # compressed buffer, so group g + 1 is copied on a second stream while
+    # group g is restored
+    ngroups = 4 if nl % 4 == 0 else 1
+    per = nl // ngroups
+    sizes = [sum(calib.stream_bytes(layer0 + l, k, T) for k in w.kv)
+             for l in range(nl)]
     offs = [0]
     for sz in sizes:
         offs.append(offs[-1] + sz)
     copy_stream = torch.cuda.Stream()
     evs = [torch.cuda.Event() for _ in range(ngroups)]
+    nk = len(w.kv)
     a.record(stream)
     for _ in range(steps):
         copy_stream.wait_event(a)
@@ -622,34 +808,15 @@ def run_e2e(kv, torch, calib, w, comp, out, x, total, stream, steps):
                     host_comp[offs[l0]:offs[l1]], non_blocking=True)
                 evs[g].record(copy_stream)
             stream.wait_event(evs[g])
-            nk = len(w.kv)
-            kv.kvtc_decompress(calib, l0, per, 3,
+            kv.kvtc_decompress(calib, layer0 + l0, per, 3,
                                dev_comp[offs[l0]:offs[l1]],
                                offs[l1] - offs[l0], T,
                                out[nk * l0:nk * l1], D, stream)
-        kv.kvtc_device_status(calib, stream)  # syncs, reads the flags back
+        kv.kvtc_device_status(calib, stream)
     b.record(stream)
     torch.cuda.synchronize()
-    t_dec = a.elapsed_time(b) / 1e3
-    # decompress direction, zero copy: kvtc_decompress reads the compressed
-    # streams straight from the pinned host buffer (mapped into the GPU's
-    # address space) over NVLink-C2C, so the transfer overlaps the
-    # reconstruction inside the kernel.  L2 is flushed before each step, so
-    # no input byte is served from a previous step's cache.
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-    zc = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
-          for _ in range(steps)]
-    for i in range(steps):
-        flush.zero_()
-        zc[i][0].record(stream)
-        kv.kvtc_decompress(calib, 0, w.layers, 3, host_comp, total, T, out, D,
-                           stream)
-        kv.kvtc_device_status(calib, stream)  # syncs, reads the flags back
-        zc[i][1].record(stream)
-    torch.cuda.synchronize()
-    t_zc = sum(e[0].elapsed_time(e[1]) for e in zc) / 1e3
-    del flush
-    # compress direction
+    t_pipe = a.elapsed_time(b) / 1e3
+    # compress direction: raw KV from pinned host memory, streams read back
     host_x = [torch.empty((T, D), dtype=torch.bfloat16, pin_memory=True)
               for _ in x]
     for h, d in zip(host_x, x):
@@ -660,57 +827,54 @@ def run_e2e(kv, torch, calib, w, comp, out, x, total, stream, steps):
     for _ in range(steps):
         for h, d in zip(host_x, dev_x):
             d.copy_(h, non_blocking=True)
-        kv.kvtc_compress(calib, 0, w.layers, 3, dev_x, D, T, dev_comp, total,
+        kv.kvtc_compress(calib, layer0, nl, 3, dev_x, D, T, dev_comp, total,
                          stream)
         host_comp.copy_(dev_comp, non_blocking=True)
     b.record(stream)
     torch.cuda.synchronize()
     t_comp = a.elapsed_time(b) / 1e3
-    del flags
-    v_pipe = raw_kv * steps / t_dec / 1e9
-    v_zc = raw_kv * steps / t_zc / 1e9
-    return {"value": max(v_pipe, v_zc), "unit": "GB/s",
-            "mode": "zero copy" if v_zc >= v_pipe else "pipelined copy",
+    return {"_seconds": t_zc, "_steps": steps,
+            "unit": "GB/s", "mode": "zero copy",
             "h2d_bytes_per_step": total, "d2h_bytes_per_step": 4,
-            "zero_copy_value": v_zc,
-            "pipelined_copy_value": v_pipe,
-            "serial_value": raw_kv * steps / t_serial / 1e9,
-            "pipeline": f"{ngroups} groups of {per} layers: the H2D copy of a "
-                        "group on a second stream overlaps the restore of the "
-                        "previous one (serial_value: copy all, then restore)",
-            "zero_copy": "kvtc_decompress given the pinned host buffer: the "
-                         "kernels read it over the host link, L2 flushed "
-                         "before each step",
-            "what": "restore: compressed streams from pinned host memory "
-                    "into device KV through kvtc_decompress, status word "
-                    "read back; value = the faster of the two modes",
+            "what": "restore: compressed streams in pinned host memory, "
+                    "read by the kernels over the host link during "
+                    "kvtc_decompress (zero copy, the mode fixed in advance), "
+                    "L2 flushed before each step, status word read back",
+            "other_modes": {
+                "pipelined_copy": {
+                    "value": raw_kv * steps / t_pipe / 1e9,
+                    "how": f"{ngroups} groups of {per} layers: the H2D copy "
+                           f"of a group on a second stream overlaps the "
+                           f"restore of the previous one"},
+                "serial_copy": {"value": raw_kv * steps / t_serial / 1e9,
+                                "how": "copy all, then restore"}},
             "compress": {"value": raw_kv * steps / t_comp / 1e9,
                          "unit": "GB/s", "h2d_bytes_per_step": raw_kv,
                          "d2h_bytes_per_step": total}}
 
 
-def run_fieldpack(kv, torch, calib, w, comp, out, total, stream, steps):
+def run_fieldpack(kv, torch, calib, w, layer0, nl, comp, out, total, stream,
+                  steps):
     """The lossless field-packing stage on the compressed streams: packed
     size, pack and unpack throughput on the device, restore from packed
     bytes (unpack, then decompress), and that restore end to end from pinned
     host memory (the packed bytes of a group of layers copied on a second
     stream while the previous group is restored)."""
     T, D = w.tokens, w.D
-    streams = w.streams()
-    n = len(streams)
-    bound = kv.kvtc_fields_bound(calib, 0, w.layers, 3, T)
-    ws = kv.kvtc_fields_workspace_bytes(calib, 0, w.layers, 3)
+    n = nl * len(w.kv)
+    bound = kv.kvtc_fields_bound(calib, layer0, nl, 3, T)
+    ws = kv.kvtc_fields_workspace_bytes(calib, layer0, nl, 3)
     packed = torch.empty(bound, dtype=torch.uint8, device="cuda")
     offs = torch.empty(n + 1, dtype=torch.int64, device="cuda")
     work = torch.empty(ws, dtype=torch.uint8, device="cuda")
     back = torch.empty_like(comp)
 
     def pack():
-        kv.kvtc_fields_pack(calib, 0, w.layers, 3, comp, total, T, packed,
+        kv.kvtc_fields_pack(calib, layer0, nl, 3, comp, total, T, packed,
                             bound, offs, work, ws, stream)
 
     def unpack(dst=back):
-        kv.kvtc_fields_unpack(calib, 0, w.layers, 3, packed, bound, offs, T,
+        kv.kvtc_fields_unpack(calib, layer0, nl, 3, packed, bound, offs, T,
                               dst, total, stream)
 
     for _ in range(3):
@@ -744,7 +908,7 @@ def run_fieldpack(kv, torch, calib, w, comp, out, total, stream, steps):
 
     def restore():
         unpack()
-        kv.kvtc_decompress(calib, 0, w.layers, 3, back, total, T, out, D,
+        kv.kvtc_decompress(calib, layer0, nl, 3, back, total, T, out, D,
                            stream)
 
     t_restore = timed(restore)
@@ -758,12 +922,13 @@ def run_fieldpack(kv, torch, calib, w, comp, out, total, stream, steps):
     host_p.copy_(packed[:P])
     dev_p = torch.empty(bound, dtype=torch.uint8, device="cuda")
     dev_offs = offs.clone()
-    ngroups = 4 if w.layers % 4 == 0 else 1
-    per = w.layers // ngroups
+    ngroups = 4 if nl % 4 == 0 else 1
+    per = nl // ngroups
     nk = len(w.kv)
     cs = [0]
-    for l in range(w.layers):
-        cs.append(cs[-1] + sum(calib.stream_bytes(l, k, T) for k in w.kv))
+    for l in range(nl):
+        cs.append(cs[-1] + sum(calib.stream_bytes(layer0 + l, k, T)
+                               for k in w.kv))
     copy_stream = torch.cuda.Stream()
     evs = [torch.cuda.Event() for _ in range(ngroups)]
     a = torch.cuda.Event(enable_timing=True)
@@ -779,12 +944,12 @@ def run_fieldpack(kv, torch, calib, w, comp, out, total, stream, steps):
                 dev_p[p0:p1].copy_(host_p[p0:p1], non_blocking=True)
                 evs[g].record(copy_stream)
             stream.wait_event(evs[g])
-            kv.kvtc_fields_unpack(calib, l0, per, 3, dev_p, bound,
+            kv.kvtc_fields_unpack(calib, layer0 + l0, per, 3, dev_p, bound,
                                   dev_offs[nk * l0:], T, back[cs[l0]:cs[l1]],
                                   cs[l1] - cs[l0], stream)
-            kv.kvtc_decompress(calib, l0, per, 3, back[cs[l0]:cs[l1]],
-                               cs[l1] - cs[l0], T, out[nk * l0:nk * l1], D,
-                               stream)
+            kv.kvtc_decompress(calib, layer0 + l0, per, 3,
+                               back[cs[l0]:cs[l1]], cs[l1] - cs[l0], T,
+                               out[nk * l0:nk * l1], D, stream)
         kv.kvtc_device_status(calib, stream)  # syncs, reads the flags back
     b.record(stream)
     torch.cuda.synchronize()

@@ -753,6 +753,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
   uint64_t* rec_full = acc_full + 5;  // [2 buffers][4 quadrants]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 32);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 33);
+  // tokens whose fields left the fp16 range, per lane quadrant: three tile
+  // slots in rotation [3][4]
+  uint32_t* range_mask = reinterpret_cast<uint32_t*>(bar + 34);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -775,6 +778,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
     for (int i = 0; i < 8; ++i) mbar_init(&rec_full[i], 4);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
+    for (int i = 0; i < 12; ++i) range_mask[i] = 0u;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -948,6 +952,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
       const int row0 = tile * kPairM + (int)rank * kTileM + q * 32;
       const int nvalid = min(max(g.tc - row0, 0), 32);
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + accb * 256u;
+      // Range masks rotate over three slots.  Set 0 clears the slot of tile
+      // it + 1 here: that slot last held tile it - 2, whose records every set
+      // has written before arriving for tile it - 1 (which set 0 has waited
+      // for), and no set can mark tile it + 1 before passing tile it's
+      // barrier, which waits for this warp.
+      const uint32_t mslot = it % 3u;
+      if (set == 0 && lane == 0)
+        range_mask[((it + 1u) % 3u) * 4u + (uint32_t)q] = 0u;
       if ((int)set == (Ga ? (Ga - 1) / gq : 0)) {
         // the warp coding the last group zeroes the record's padding:
         // fields and planes cover bytes [0, used) exactly
@@ -999,9 +1011,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
           const float lev = (float)((1 << b) - 1);
           const __half sh = __float2half_rd(lo);
           const float shf = __half2float(sh);
-          // upper bound of (hi - shift) / lev, then rounded up to fp16
-          const float pre = __fmul_ru(__fsub_ru(hi, shf), __frcp_ru(lev));
-          const __half sc = __float2half_ru(pre);
+          // scale = the least fp16 s with s * lev >= hi - shift: an upper
+          // bound of the quotient rounded up to fp16 lands on s or on the
+          // fp16 value after it; the product of the value before with lev
+          // (at most 11 + 8 significant bits) is exact in fp32, so one
+          // comparison settles which
+          const float dif = __fsub_ru(hi, shf);
+          __half sc = __float2half_ru(__fmul_ru(dif, __frcp_ru(lev)));
+          {
+            const unsigned short sb = __half_as_ushort(sc);
+            if (sb > 0u && sb < 0x7C00u) {
+              const __half below = __ushort_as_half((unsigned short)(sb - 1u));
+              if (__half2float(below) * lev >= dif) sc = below;
+            }
+          }
           const float scf = __half2float(sc);
           range_err |= __hisinf(sh) != 0 || __hisinf(sc) != 0 ||
                        __hisnan(sh) || __hisnan(sc);
@@ -1034,23 +1057,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
           }
         }
       }
-      if (range_err && lane < nvalid) atomicOr(p.status, KVTC_FLAG_RANGE);
+      // a token whose fields left the fp16 range raises the sticky flag and
+      // its record is not written
+      const uint32_t bad = __ballot_sync(0xFFFFFFFFu, range_err && lane < nvalid);
+      if (bad && lane == 0) {
+        atomicOr(p.status, KVTC_FLAG_RANGE);
+        atomicOr(&range_mask[mslot * 4u + (uint32_t)q], bad);
+      }
       __syncwarp();
       KVTC_TR(2)
-      // both warps of the quadrant have staged their groups
+      // all four warps of the quadrant have staged their groups
       if (lane == 0) mbar_arrive(&rec_full[accb * 4u + (uint32_t)q]);
       if (!mbar_wait(&rec_full[accb * 4u + (uint32_t)q], (it >> 1) & 1u,
                      abort_flag)) {
         ok = false;
         break;
       }
+      const uint32_t skip =
+          *reinterpret_cast<volatile uint32_t*>(&range_mask[mslot * 4u + (uint32_t)q]);
       // set s writes tokens [8 s, 8 s + 8) of the quadrant
       uint8_t* rbase = g.rec + (int64_t)row0 * R;
       const int o_end = (int)(set + 1) * 8 * R;
       for (int o = (int)set * 8 * R + lane * 16; o < o_end; o += 512) {
         const int tr = o / R;
         const int wd = (o - tr * R) >> 2;
-        if (tr < nvalid)
+        if (tr < nvalid && !((skip >> tr) & 1u))
           st_v4(rbase + o, stg[wd * 33 + tr], stg[(wd + 1) * 33 + tr],
                 stg[(wd + 2) * 33 + tr], stg[(wd + 3) * 33 + tr]);
       }

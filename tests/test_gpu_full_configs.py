@@ -22,7 +22,7 @@ import synth
 from oracle import codec
 
 from _parity import (blob_for, calibrate_workload, check_decompress,
-                     check_records, stream_calibs)
+                     check_records, record, stream_calibs)
 
 pytestmark = pytest.mark.gpu
 
@@ -54,6 +54,7 @@ def check_stream_records(g: bytes, x: np.ndarray, sc_enc, T, w):
     assert g[:raw] == o_raw, "raw rows differ"
     grec = np.frombuffer(g, np.uint8, tc * sc_enc.R, raw).reshape(tc, sc_enc.R)
     st = check_records(grec, x[s_:T - w_], sc_enc)
+    record(w.name, st=st)
     assert st["bad"] == 0, st
 
 
@@ -63,6 +64,7 @@ def check_stream_restore(got: np.ndarray, oracle_bytes: bytes, T, sc_dec, w):
     np.testing.assert_array_equal(got[:s_], ref[:s_])
     np.testing.assert_array_equal(got[T - w_:], ref[T - w_:])
     st = check_decompress(got[s_:T - w_], ref[s_:T - w_])
+    record(w.name, dst=st)
     assert st["ok"], st
 
 

@@ -6,7 +6,7 @@ import synth
 from oracle import codec, fp
 
 from _parity import (blob_for, calibrate_workload, check_decompress,
-                     check_records, stream_calibs)
+                     check_records, record, stream_calibs)
 
 pytestmark = pytest.mark.gpu
 
@@ -80,6 +80,7 @@ def run_roundtrip(kv, torch, name, streams, T, ld_pad=0, sample=None):
         rows = np.arange(tc) if sample is None else sample(tc)
         grec = np.frombuffer(g, np.uint8, tc * R, raw).reshape(tc, R)[rows]
         st = check_records(grec, xs[(l, k)][s_ + rows], sc_enc)
+        record(name, st=st)
         assert st["bad"] == 0, st
         stats.append(st)
         oracle_stream[(l, k)] = o
@@ -103,6 +104,7 @@ def run_roundtrip(kv, torch, name, streams, T, ld_pad=0, sample=None):
         np.testing.assert_array_equal(got[:s_], ref[:s_])
         np.testing.assert_array_equal(got[T - w_:], ref[T - w_:])
         st = check_decompress(got[s_:T - w_], ref[s_:T - w_])
+        record(name, dst=st)
         assert st["ok"], st
         dstats.append(st)
         if ld_pad:  # padding columns untouched
@@ -208,6 +210,7 @@ def run_paged(kv, torch, name, streams, Ts):
             np.testing.assert_array_equal(got[:s_], ref[:s_])
             np.testing.assert_array_equal(got[T - w_:], ref[T - w_:])
             st = check_decompress(got[s_:T - w_], ref[s_:T - w_])
+            record(name + " (paged)", dst=st)
             assert st["ok"], st
     # untouched blocks keep their contents
     used = set(table[r, t] for r, T in enumerate(Ts)
@@ -346,6 +349,7 @@ def test_full_llama31_8b_8k_sampled(kv, torch):
         grec = np.frombuffer(g, np.uint8, tc * sc_enc.R, raw).reshape(
             tc, sc_enc.R)
         st = check_records(grec, x[s_:T - w_], sc_enc)
+        record(name, st=st)
         assert st["bad"] == 0, (idx, st)
         # GPU decompress of the GPU bitstream vs the oracle decompressing
         # the same bitstream
@@ -354,6 +358,7 @@ def test_full_llama31_8b_8k_sampled(kv, torch):
         np.testing.assert_array_equal(got[:s_], x[:s_])
         np.testing.assert_array_equal(got[T - w_:], x[T - w_:])
         dst = check_decompress(got[s_:T - w_], ref[s_:T - w_])
+        record(name, dst=dst)
         assert dst["ok"], (idx, dst)
         worst = max(worst, dst["rel_l2"])
     calib.free()
