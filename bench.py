@@ -691,6 +691,12 @@ def overlap_schedule(kv, torch, calib, w, layer0, nl, comp, out, total,
     cons = torch.cuda.Stream() if overlapped else stream
     for e in evs + done + [start]:
         e.record(stream)
+    # the consumer once on each stream beforehand: the first use of a
+    # library GEMM on a stream sets it up on the host, which must not fall
+    # into the timed window
+    for st in {stream, cons}:
+        with torch.cuda.stream(st):
+            attention_stand_in(torch, out[0], out[1], q)
     torch.cuda.synchronize()
     torch.cuda._sleep(40_000_000)
     start.record(stream)

@@ -96,9 +96,15 @@ typedef struct kvtc_calib kvtc_calib;
  *                      with kvtc_calib_free).
  * Derived on load: bf16 V_kept (projection), fp16 V_kept (reconstruction),
  * fp32 mu and fp32 m = bf16(V_kept) mu, group layout tables, TMA
- * descriptors.  Requirements: D % 64 == 0, D <= 8192, k <= 240 (the
- * reconstruction contracts k plus one mean step of 16 over at most 256
- * columns), record bytes <= 256; otherwise ENOTSUP.
+ * descriptors.  Requirements: D % 64 == 0, D <= 8192, 16 <= k <= 496 (the
+ * reconstruction holds k plus one mean step of 16 fp16 columns in 256
+ * tensor-memory columns), record bytes <= 256, and the projection's
+ * two-stage shared-memory ring fits beside its record staging
+ * (2 (32768 + 128 k) + 264 R + 1344 <= 232448 bytes, R the record bytes);
+ * otherwise ENOTSUP.  Up to k = 240 both kernels double-buffer their
+ * tensor-memory operands; above, a launch that holds such a stream
+ * single-buffers them (the projection above k = 256, the reconstruction's
+ * A operand above k = 240).
  * Errors: EINVAL, EFORMAT, ENOMEM, ECUDA, ENOTSUP.
  */
 int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
@@ -198,6 +204,10 @@ int kvtc_decompress_paged(const kvtc_calib* calib, int layer0, int nlayers,
  *   bytes, so a packed stream is never longer than the codec stream plus
  *   its header and table.  Streams are concatenated in (layer, K, V) order.
  */
+
+/* Field packing holds one field slot per lane of a warp: every selected
+ * stream must keep at most 15 groups (k <= 240), else the three calls below
+ * return ENOTSUP. */
 
 /* Upper bound on the packed bytes of the selected streams at T tokens
  * (< 0 on error). */

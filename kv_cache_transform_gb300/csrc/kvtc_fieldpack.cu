@@ -40,7 +40,7 @@ namespace kvtc {
 namespace {
 
 static_assert(kFpChunks == 8, "layout pass reads 8 chunks x 4 lanes");
-static_assert(kMaxK / 16 <= 15, "at most 30 field slots (one warp)");
+static_assert(kNarrowK / 16 <= 15, "at most 30 field slots (one warp)");
 constexpr int kFpThreads = 256;
 constexpr int kFpWarps = kFpThreads / 32;
 constexpr int kFpLayoutThreads = 1024;

@@ -214,6 +214,21 @@ namespace {
 
 int record_bytes(int budget_bits) { return 16 * ((budget_bits + 127) / 128); }
 
+// Row of V_enc (K-block major [D/64][k][64]) that holds kept component a.
+// CTA r of a pair loads rows [r k/2, (r + 1) k/2).  Up to k = 256 one MMA
+// of N = k reads them in order.  Above, two MMAs per K step read rows
+// [0, 128) (N = 256, output columns [0, 256)) and rows [128, k/2)
+// (N = k - 256, columns [256, k)) of each CTA, so the rows are stored in
+// the order that puts component j in output column j.
+int venc_row(int a, int k) {
+  if (k <= 256) return a;
+  const int half = k / 2, h2 = (k - 256) / 2;
+  if (a < 128) return a;
+  if (a < 256) return half + (a - 128);
+  if (a < 256 + h2) return 128 + (a - 256);
+  return half + 128 + (a - 256 - h2);
+}
+
 void split_tokens(int64_t T, int s, int w, int64_t* s_, int64_t* w_,
                   int64_t* tc) {
   *s_ = std::min<int64_t>(s, T);
@@ -393,8 +408,12 @@ int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
     }
     h.Ga = ga;
     h.R = R;
+    // the projection's two-stage ring (x tile and this CTA's V_enc half,
+    // two K blocks each) and its record staging must fit shared memory
+    const bool smem_ok =
+        compress_smem_bytes(2, 2 * kTileM * 128 + h.k * 128, R / 4) <= 232448;
     if (h.D % 64 || h.D > kMaxD || h.k > kMaxK || h.k == 0 || R > kMaxRecord ||
-        find_stream(c, h.layer, h.kv) >= 0) {
+        !smem_ok || find_stream(c, h.layer, h.kv) >= 0) {
       status = find_stream(c, h.layer, h.kv) >= 0 ? KVTC_EFORMAT : KVTC_ENOTSUP;
       break;
     }
@@ -479,7 +498,8 @@ int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
         double v;
         std::memcpy(&v, V + (size_t)a * h.D + d, 8);
         const uint16_t eb = bf16_bits_rne(v);
-        venc[((size_t)(d >> 6) * h.k + a) * 64 + (d & 63)] = eb;
+        venc[((size_t)(d >> 6) * h.k + venc_row(a, h.k)) * 64 + (d & 63)] =
+            eb;
         vd(d, a) = fp16_bits_rne(v);
         uint32_t u = (uint32_t)eb << 16;
         float ef;
@@ -511,13 +531,17 @@ int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
     s.R = h.R;
     s.nc = (h.D % 256 == 0) ? 256 : (h.D % 128 == 0) ? 128 : 64;
     s.kp = kp;
+    // the reconstruction's B operand comes in one ring stage per chunk
+    // (every K block, at most four) or in two
+    const int nkb = (kp + 63) / 64;
+    s.nbs = nkb <= 4 ? 1 : 2;
+    s.kbs = (nkb + s.nbs - 1) / s.nbs;
     // each CTA of a pair loads half of the N rows of the B operand, several K
-    // blocks at once (V_dec: every K block of a chunk half; V_enc: two K
+    // blocks at once (V_dec: kbs K blocks of a chunk half; V_enc: two K
     // blocks of the component half)
     if (!encode_blocked_3d(&s.tm_vdec, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                           dev + o.vdec, (uint64_t)h.D,
-                           (uint64_t)((kp + 63) / 64), (uint32_t)(s.nc / 2),
-                           (uint32_t)((kp + 63) / 64)) ||
+                           dev + o.vdec, (uint64_t)h.D, (uint64_t)nkb,
+                           (uint32_t)(s.nc / 2), (uint32_t)s.kbs) ||
         !encode_blocked_3d(&s.tm_venc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                            dev + o.venc, (uint64_t)h.k, (uint64_t)(h.D / 64),
                            (uint32_t)(h.k / 2), 2u)) {
@@ -688,6 +712,7 @@ int kvtc_compress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
       rmax = std::max(rmax, h.R);
     }
     if (ret != KVTC_OK) break;
+    p->wide = kmax > 256;
     p->streams = c->d_streams;
     p->status = c->d_status;
     p->nseg = (int32_t)(i1 - i0);
@@ -835,9 +860,13 @@ int kvtc_decompress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
       p->nseg = (int32_t)(i1 - i0);
       p->total_tiles = tiles;
       p->tiles_per_seg = (int32_t)((tc + kPairM - 1) / kPairM);
-      int rmax = 0;
-      for (size_t i = i0; i < i1; ++i) rmax = std::max(rmax, c->hs[cs[i]].R);
+      int rmax = 0, kmax = 0;
+      for (size_t i = i0; i < i1; ++i) {
+        rmax = std::max(rmax, c->hs[cs[i]].R);
+        kmax = std::max(kmax, c->hs[cs[i]].k);
+      }
       p->rec_words = rmax / 4;
+      p->wide = kmax > kNarrowK;
       p->nstages = decompress_stages(p->rec_words);
       const int mp = max_pairs_decompress(
           decompress_smem_bytes(p->nstages, p->rec_words));
@@ -931,9 +960,13 @@ int kvtc_decompress_paged(const kvtc_calib* c, int layer0, int nlayers,
     p->total_tiles = tiles;
     p->D = D;
     p->total_raw_chunks = raw_chunks;
-    int rmax = 0;
-    for (size_t j = 0; j < cs.size(); ++j) rmax = std::max(rmax, c->hs[cs[j]].R);
+    int rmax = 0, kmax = 0;
+    for (size_t j = 0; j < cs.size(); ++j) {
+      rmax = std::max(rmax, c->hs[cs[j]].R);
+      kmax = std::max(kmax, c->hs[cs[j]].k);
+    }
     p->rec_words = rmax / 4;
+    p->wide = kmax > kNarrowK;
     p->nstages = decompress_stages(p->rec_words);
     if (launch_paged_raw(*p, stream) != cudaSuccess) ret = KVTC_ECUDA;
     const int mp =
@@ -1001,14 +1034,23 @@ void fp_fill(FpParams* p, const kvtc_calib* c, const std::vector<int>& cs,
   p->total_items = items;
 }
 
+// Field packing holds one field slot per lane of a warp: at most 15 active
+// groups (30 slots) per stream.
+int fp_supported(const kvtc_calib* c, const std::vector<int>& cs) {
+  for (int i : cs)
+    if (c->hs[i].Ga > 15) return KVTC_ENOTSUP;
+  return KVTC_OK;
+}
+
 }  // namespace
 
 int64_t kvtc_fields_bound(const kvtc_calib* c, int layer0, int nlayers,
                           int kv_mask, int64_t T) {
   if (!c || T < 0 || T > (1LL << 31) - 1) return KVTC_EINVAL;
   std::vector<int> cs, slot;
-  const int st = select_streams(c, layer0, nlayers, kv_mask, &cs, &slot);
+  int st = select_streams(c, layer0, nlayers, kv_mask, &cs, &slot);
   if (st != KVTC_OK) return st;
+  if ((st = fp_supported(c, cs)) != KVTC_OK) return st;
   int64_t n = 0;
   for (int i : cs) n += fp_bound_of(c, c->hs[i], T);
   return n;
@@ -1035,6 +1077,7 @@ int kvtc_fields_pack(const kvtc_calib* c, int layer0, int nlayers,
   int st = select_streams(c, layer0, nlayers, kv_mask, &cs, &slot);
   if (st != KVTC_OK) return st;
   if (cs.empty()) return KVTC_EINVAL;
+  if ((st = fp_supported(c, cs)) != KVTC_OK) return st;
   std::vector<int64_t> off(cs.size());
   int64_t need = 0, bound = 0;
   for (size_t i = 0; i < cs.size(); ++i) {
@@ -1082,6 +1125,7 @@ int kvtc_fields_unpack(const kvtc_calib* c, int layer0, int nlayers,
   int st = select_streams(c, layer0, nlayers, kv_mask, &cs, &slot);
   if (st != KVTC_OK) return st;
   if (cs.empty()) return KVTC_EINVAL;
+  if ((st = fp_supported(c, cs)) != KVTC_OK) return st;
   std::vector<int64_t> off(cs.size());
   int64_t need = 0;
   for (size_t i = 0; i < cs.size(); ++i) {

@@ -10,7 +10,13 @@ constexpr int kGroup = 16;         // components per microscaling group
 constexpr int kTileM = 128;        // tokens per CTA tile (TMEM lanes)
 constexpr int kPairM = 256;        // tokens per CTA-pair super-tile (MMA M)
 constexpr int kAtomK = 64;         // 16-bit elements per 128-byte swizzle row
-constexpr int kMaxK = 240;         // kept components supported
+constexpr int kMaxK = 496;         // kept components supported (TMEM: the
+                                   // decompress A operand, k + 16 fp16
+                                   // columns, in 256 TMEM columns)
+constexpr int kNarrowK = 240;      // up to here both kernels double-buffer
+                                   // (compress: k <= 256 accumulators of
+                                   // 256 columns; decompress: A buffers of
+                                   // 128 columns hold k + 16 <= 256)
 constexpr int kMaxRecord = 256;    // record bytes supported by the kernels
 constexpr int kMaxD = 8192;
 
@@ -29,7 +35,8 @@ struct DevStream {
   int32_t D, k, Ga, R;      // R = record bytes
   int32_t nc;               // reconstruction N chunk: 256, 128 or 64
   int32_t kp;               // reconstruction K: k + 16 (the mean step)
-  int32_t pad[2];
+  int32_t kbs;              // reconstruction: K blocks per B ring stage
+  int32_t nbs;              // reconstruction: B ring stages per chunk
 };
 
 // Raw rows (sink and window) copied by two warps of a tensor-core kernel
@@ -73,6 +80,10 @@ struct CompParams {
   int32_t stage_bytes;      // A + B bytes of one stage (two K blocks)
   int32_t b_bytes_max;      // B bytes reserved per stage
   int32_t rec_stg_words;    // record staging words per thread
+  int32_t wide;             // a stream keeps k > 256: one k-column
+                            // accumulator, two MMAs (N = 256, k - 256) per
+                            // K step
+  int32_t pad2;
   RawList raw;              // sink/window rows and padding of these streams
 };
 
@@ -95,6 +106,8 @@ struct DecParams {
   int32_t tiles_per_seg;    // every stream of a call has the same T
   int32_t nstages;          // B ring depth (shared-memory stages)
   int32_t rec_words;        // record staging words per thread (max R / 4)
+  int32_t wide;             // a stream has k + 16 > 256: one A buffer
+  int32_t pad2;
   RawList raw;              // sink/window rows of these streams
 };
 // every stream's sink, window and padding segments fit one launch's list
@@ -128,6 +141,7 @@ struct PagedParams {
   int64_t total_raw_chunks;
   int32_t nstages;          // B ring depth (shared-memory stages)
   int32_t rec_words;        // record staging words per thread (max R / 4)
+  int32_t wide;             // a stream has k + 16 > 256: one A buffer
 };
 
 // ---------------------------------------------------------------- raw rows

@@ -196,8 +196,10 @@ constexpr int kDecWarps = 28;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kDecMaxNC = 256;  // widest output chunk (one MMA's N)
 constexpr int kDecMaxStages = 8;
-// one B stage = this CTA's half of a chunk, every K block: [kb][nc/2][64]
-constexpr int kDecBStage = (kDecMaxNC / 2) * 128 * (kMaxK / 64 + 1);
+// one B stage = this CTA's half of a chunk, up to four K blocks:
+// [kbs][nc/2][64]; a chunk takes one stage (k + 16 <= 256) or two
+constexpr int kDecMaxKbs = 4;
+constexpr int kDecBStage = (kDecMaxNC / 2) * 128 * kDecMaxKbs;
 constexpr int kDecStgWarp = 32 * 128;  // 32 rows x 64 bf16, SW128
 constexpr int kDecBarBytes = 512;
 // Shared memory: [B ring: nstages x 64 KB][staging: 16 warps x 4 KB]
@@ -363,27 +365,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         const DecTile t = resolve(p, item);
         const DevStream* ds = p.streams + t.cs;
         const int nc = ds->nc, nch = ds->D / nc, half = nc >> 1;
-        const int nkb = (ds->kp + kAtomK - 1) / kAtomK;
-        // both halves of the chunk, every K block
-        const uint32_t bytes_pair = (uint32_t)nc * 128u * (uint32_t)nkb;
+        const int kbs = ds->kbs, nbs = ds->nbs;
+        // both halves of the chunk, kbs K blocks (a box past the last K
+        // block is filled with zeros and still counts its full bytes)
+        const uint32_t bytes_pair = (uint32_t)nc * 128u * (uint32_t)kbs;
         if (item == pair) prefetch_tmap(&ds->tm_vdec);
-        for (int ch = 0; ch < nch; ++ch) {
-          KVTC_TR(0)
-          if (!mbar_wait(&empty_b[s], ph ^ 1u, abort_flag)) {
-            ok = false;
-            break;
+        for (int ch = 0; ch < nch && ok; ++ch) {
+          for (int h = 0; h < nbs; ++h) {
+            KVTC_TR(0)
+            if (!mbar_wait(&empty_b[s], ph ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (leader) mbar_arrive_expect_tx(&full_b[s], bytes_pair);
+            KVTC_TR(1)
+            tma_load_3d_pair(sB + s * kDecBStage, &ds->tm_vdec, 0,
+                             ch * nc + (int)rank * half, h * kbs,
+                             full_leader + s * 8u);
+            ++it_b;
+            if (++s == (uint32_t)nst) {
+              s = 0;
+              ph ^= 1u;
+            }
+            KVTC_TR(2)
           }
-          if (leader) mbar_arrive_expect_tx(&full_b[s], bytes_pair);
-          KVTC_TR(1)
-          tma_load_3d_pair(sB + s * kDecBStage, &ds->tm_vdec, 0,
-                           ch * nc + (int)rank * half, 0,
-                           full_leader + s * 8u);
-          ++it_b;
-          if (++s == (uint32_t)nst) {
-            s = 0;
-            ph ^= 1u;
-          }
-          KVTC_TR(2)
         }
       }
       KVTC_TR(0)
@@ -417,10 +422,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         const uint32_t nbm = (1u << lg) - 1u;
         const int ksteps = ds->kp / kGroup;  // kept groups + the mean step
         const int kb_units = (ds->nc / 2) * 128 / 16;  // one K block, >> 4
+        const int sstep = 4 * ds->kbs;       // K steps per B stage
+        const int nbs = ds->nbs;
         const uint32_t idesc = make_idesc(256, (uint32_t)nc, 0);
-        const uint32_t abuf = it & 1u;
+        // A buffers: two of 128 columns, or one of 256 (wide launch)
+        const uint32_t abuf = p.wide ? 0u : it & 1u;
+        const uint32_t ause = p.wide ? it : it >> 1;
         KVTC_TR(0)
-        if (!mbar_wait(&a_full[abuf], (it >> 1) & 1u, abort_flag)) {
+        if (!mbar_wait(&a_full[abuf], ause & 1u, abort_flag)) {
           ok = false;
           break;
         }
@@ -438,42 +447,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
           }
           KVTC_TR(2)
           const uint32_t d = tmem + accb * (uint32_t)nc;
-          KVTC_TR(0)
-          if (!b_ready && !mbar_wait(&full_b[s], ph, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          KVTC_TR(3)
-          // K block kb of this CTA's half lies at kb * half * 128 bytes; the
-          // descriptor start address advances 32 bytes (2 units) per K=16.
-          // The tensor pipe queues almost nothing ahead, so the steps are
-          // one unrolled, branch-free run of predicated MMAs whose operands
-          // are all simple offsets of two registers.
-          const uint64_t bdesc = desc_b0 + (uint64_t)(s * (kDecBStage >> 4));
-          // the next chunk's barriers are tested (never waited on) right
-          // after the first MMA, so the test overlaps the MMA run
-          const uint32_t s_next = s + 1 == (uint32_t)nst ? 0u : s + 1;
-          const uint32_t ph_next = s + 1 == (uint32_t)nst ? ph ^ 1u : ph;
           const uint32_t c_next = chunk + 1;
-#pragma unroll
-          for (int step = 0; step < kMaxK / kGroup + 1; ++step) {
-            mma_ts_pair_if(d, a_col + (uint32_t)step * 8u,
-                           bdesc + (uint64_t)((step >> 2) * kb_units +
-                                              (step & 3) * 2),
-                           idesc, step > 0, step < ksteps);
-            if (step == 0) {
-              acc_ready = mbar_test_wait(&acc_empty[c_next & nbm],
-                                         ((c_next >> lg) & 1u) ^ 1u);
-              b_ready = mbar_test_wait(&full_b[s_next], ph_next);
+          for (int h = 0; h < nbs; ++h) {
+            KVTC_TR(0)
+            if (!b_ready && !mbar_wait(&full_b[s], ph, abort_flag)) {
+              ok = false;
+              break;
             }
+            tc_fence_after();
+            KVTC_TR(3)
+            // K block kb of this stage lies at kb * half * 128 bytes; the
+            // descriptor start address advances 32 bytes (2 units) per
+            // K=16.  The tensor pipe queues almost nothing ahead, so a
+            // stage's steps are one unrolled, branch-free run of predicated
+            // MMAs whose operands are all simple offsets of two registers.
+            const uint64_t bdesc =
+                desc_b0 + (uint64_t)(s * (kDecBStage >> 4));
+            const int step0 = h * sstep;
+            const int nsteps = min(ksteps - step0, sstep);
+            const uint32_t a_h = a_col + (uint32_t)step0 * 8u;
+            // the next stage's and the next chunk's barriers are tested
+            // (never waited on) right after the first MMA, so the test
+            // overlaps the MMA run
+            const uint32_t s_next = s + 1 == (uint32_t)nst ? 0u : s + 1;
+            const uint32_t ph_next = s + 1 == (uint32_t)nst ? ph ^ 1u : ph;
+#pragma unroll
+            for (int step = 0; step < 4 * kDecMaxKbs; ++step) {
+              mma_ts_pair_if(d, a_h + (uint32_t)step * 8u,
+                             bdesc + (uint64_t)((step >> 2) * kb_units +
+                                                (step & 3) * 2),
+                             idesc, (h | step) > 0, step < nsteps);
+              if (step == 0) {
+                acc_ready = mbar_test_wait(&acc_empty[c_next & nbm],
+                                           ((c_next >> lg) & 1u) ^ 1u);
+                b_ready = mbar_test_wait(&full_b[s_next], ph_next);
+              }
+            }
+            tc_commit_pair(&empty_b[s], 3);
+            if (++s == (uint32_t)nst) {
+              s = 0;
+              ph ^= 1u;
+            }
+            KVTC_TR(4)
           }
-          tc_commit_pair(&empty_b[s], 3);
-          if (++s == (uint32_t)nst) {
-            s = 0;
-            ph ^= 1u;
-          }
-          KVTC_TR(4)
           if (!ok) break;
           tc_commit_pair(&acc_full[accb], 3);
           ++chunk;
@@ -501,12 +517,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
     bool ok = true;
     KVTC_TR_DECL
     for (int item = pair; item < total; item += npairs, ++it) {
-      const uint32_t abuf = it & 1u;
-      if (abuf != set) continue;
+      if ((it & 1u) != set) continue;
+      // A buffers: two of 128 columns, or one of 256 (wide launch)
+      const uint32_t abuf = p.wide ? 0u : it & 1u;
+      const uint32_t ause = p.wide ? it : it >> 1;
       const DecTile t = resolve(p, item);
       const DevStream* ds = p.streams + t.cs;
       const int R = ds->R, Ga = ds->Ga;
-      // group widths and plane offsets: lane a holds group a's (Ga <= 15),
+      // group widths and plane offsets: lane a holds group a's (Ga <= 31),
       // broadcast per group by shuffle
       const int my_b = lane < Ga ? (int)ds->bits[lane] : 0;
       const int my_po = lane < Ga ? (int)ds->poff[lane] : 0;
@@ -539,7 +557,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         }
       }
       KVTC_TR(2)
-      if (!mbar_wait(&a_empty[abuf], ((it >> 1) & 1u) ^ 1u, abort_flag)) {
+      if (!mbar_wait(&a_empty[abuf], (ause & 1u) ^ 1u, abort_flag)) {
         ok = false;
         break;
       }
@@ -859,12 +877,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
         const CompSeg& g = p.seg[find_comp_seg(p, item)];
         const DevStream* ds = p.streams + g.cs;
         const int nkb = ds->D / kAtomK;
-        const uint32_t idesc = make_idesc(256, (uint32_t)ds->k, 1);
+        // N = k as one MMA per K step, or for k > 256 two: N = 256 into
+        // accumulator columns [0, 256) from rows [0, 128) of each CTA's
+        // V_enc half, and N = k - 256 into [256, k) from the rows after
+        // (the rows are stored so that column j is component j)
+        const uint32_t n1 = ds->k > 256 ? 256u : (uint32_t)ds->k;
+        const uint32_t n2 = ds->k > 256 ? (uint32_t)ds->k - 256u : 0u;
+        const uint32_t idesc = make_idesc(256, n1, 1);
+        const uint32_t idesc2 = make_idesc(256, n2 ? n2 : 16u, 1);
         // one K block of this CTA's V_enc half, in 16-byte units
         const uint64_t b_kb_units = (uint64_t)((ds->k >> 1) * 128 / 16);
-        const uint32_t accb = it & 1u;
+        // double-buffered accumulators, or one of k columns (wide launch)
+        const uint32_t accb = p.wide ? 0u : it & 1u;
+        const uint32_t ause = p.wide ? it : it >> 1;
         KVTC_TR(0)
-        if (!mbar_wait(&acc_empty[accb], ((it >> 1) & 1u) ^ 1u, abort_flag)) {
+        if (!mbar_wait(&acc_empty[accb], (ause & 1u) ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
@@ -887,10 +914,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
 #pragma unroll
           for (int j = 0; j < 2; ++j)
 #pragma unroll
-            for (int st = 0; st < 4; ++st)
+            for (int st = 0; st < 4; ++st) {
               mma_ss_pair_if(d, ad + (uint64_t)j * a_kb_units + 2u * st,
                              bd + (uint64_t)j * b_kb_units + 2u * st, idesc,
                              (kb | j | st) != 0, j == 0 || two);
+              // rows [128, k/2) of the half: 128 rows x 128 B further
+              mma_ss_pair_if(d + 256u,
+                             ad + (uint64_t)j * a_kb_units + 2u * st,
+                             bd + (uint64_t)j * b_kb_units + 2u * st + 1024u,
+                             idesc2, (kb | j | st) != 0,
+                             n2 != 0 && (j == 0 || two));
+            }
           tc_commit_pair(&empty[s], 3);
           if (++s == (uint32_t)nst) {
             s = 0;
@@ -929,8 +963,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
     bool ok = true;
     KVTC_TR_DECL
     for (int item = pair; item < total; item += npairs, ++it) {
-      const uint32_t accb = it & 1u;  // accumulator and staging buffer
-      uint32_t* stg = sRec + (accb * 4u + (uint32_t)q) * (rec_words * 33);
+      // accumulator (double-buffered, or one of k columns in a wide
+      // launch) and record staging buffer (always two, alternating)
+      const uint32_t accb = p.wide ? 0u : it & 1u;
+      const uint32_t ause = p.wide ? it : it >> 1;
+      const uint32_t sb = it & 1u;
+      uint32_t* stg = sRec + (sb * 4u + (uint32_t)q) * (rec_words * 33);
       const uint32_t stg_addr = smem_u32(stg);
       const int sg = find_comp_seg(p, item);
       const CompSeg& g = p.seg[sg];
@@ -943,7 +981,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
       const int a_begin = min(Ga, (int)set * gq);
       const int a_end = min(Ga, (int)set * gq + gq);
       KVTC_TR(0)
-      if (!mbar_wait(&acc_full[accb], (it >> 1) & 1u, abort_flag)) {
+      if (!mbar_wait(&acc_full[accb], ause & 1u, abort_flag)) {
         ok = false;
         break;
       }
@@ -1067,8 +1105,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
       __syncwarp();
       KVTC_TR(2)
       // all four warps of the quadrant have staged their groups
-      if (lane == 0) mbar_arrive(&rec_full[accb * 4u + (uint32_t)q]);
-      if (!mbar_wait(&rec_full[accb * 4u + (uint32_t)q], (it >> 1) & 1u,
+      if (lane == 0) mbar_arrive(&rec_full[sb * 4u + (uint32_t)q]);
+      if (!mbar_wait(&rec_full[sb * 4u + (uint32_t)q], (it >> 1) & 1u,
                      abort_flag)) {
         ok = false;
         break;

@@ -99,6 +99,14 @@ WORKLOADS = {
                               head_dim=128, tokens=8192, requests=1, rank=128,
                               spectrum_p=1.0, outliers=True, sink=4,
                               window=128, avg_bits=1.0),
+    # config-2 shape with a flat spectrum (isotropic latent factors, no
+    # outlier channels): the DP keeps 16 two-bit groups, k = 256, the widest
+    # the 1-bit/coef budget reaches with this quantiser
+    "llama31_8b_8k_flat": Workload("llama31_8b_8k_flat", layers=32,
+                                   kv=(0, 1), heads=8, head_dim=128,
+                                   tokens=8192, requests=1, rank=1024,
+                                   spectrum_p=0.0, outliers=False, sink=4,
+                                   window=128, avg_bits=1.0),
     "mistral_nemo_12b_32k": Workload("mistral_nemo_12b_32k", layers=40,
                                      kv=(0, 1), heads=8, head_dim=128,
                                      tokens=32768, requests=1, rank=128,

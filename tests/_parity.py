@@ -113,10 +113,37 @@ def calibrate_workload(name: str, streams: Sequence[Tuple[int, int]],
                 os.environ[k] = v
 
 
-def blob_for(name: str, entries: Sequence[tuple]) -> bytes:
+def _pca_one(args):
+    name, layer, kv = args
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
     w = synth.WORKLOADS[name]
-    return calibrate.write_blob(entries, w.sink, w.window, w.budget_bits,
-                                w.bmax, w.group)
+    mu, evals, V = calibrate.pca(synth.calib_tokens(w, layer, kv))
+    return layer, kv, mu, V, evals
+
+
+def calibrate_forced(name: str, streams: Sequence[Tuple[int, int]],
+                     widths: np.ndarray) -> List[tuple]:
+    """Oracle PCA of the given streams with the group widths set by hand
+    instead of by the DP (a valid calibration the DP would not pick: it
+    reaches kept-component counts the budget allows but the allocation
+    never chooses)."""
+    jobs = [(name, l, kv) for l, kv in streams]
+    if len(jobs) <= 2:
+        out = [_pca_one(j) for j in jobs]
+    else:
+        n = min(len(jobs), os.cpu_count() or 4)
+        with cf.ProcessPoolExecutor(
+                n, mp_context=mp.get_context("spawn")) as ex:
+            out = list(ex.map(_pca_one, jobs))
+    wd = np.asarray(widths, dtype=np.int64)
+    return [(l, kv, mu, V, ev, wd) for l, kv, mu, V, ev in out]
+
+
+def blob_for(name: str, entries: Sequence[tuple],
+             budget_bits: int = None) -> bytes:
+    w = synth.WORKLOADS[name]
+    return calibrate.write_blob(entries, w.sink, w.window,
+                                budget_bits or w.budget_bits, w.bmax, w.group)
 
 
 def stream_calibs(blob: bytes):

@@ -116,14 +116,23 @@ def test_python_binding_raises_on_error(kv):
     assert e.value.code == kv.KVTC_EFORMAT
 
 
-def test_kept_components_beyond_the_kernel_limit_are_refused(kv):
-    """k = 256 kept components (every group of a D = 256 stream at width 1)
-    is a valid blob, but the reconstruction contracts k plus one mean step
-    over at most 256 columns, so the library refuses it (ENOTSUP) while
-    parsing, before any CUDA call."""
-    D = 256
+def test_kept_components_beyond_the_kernel_limits_are_refused(kv):
+    """Valid blobs the kernels cannot run are refused (ENOTSUP) while
+    parsing, before any CUDA call:
+    - k = 512 (every group of a D = 512 stream at width 1): the
+      reconstruction holds k plus one mean step of 16 fp16 columns in 256
+      TMEM columns, so k <= 496;
+    - k = 400 with 256-byte records: the projection's two-stage ring (x and
+      this CTA's 200 V_enc rows, two K blocks each) and the record staging
+      exceed shared memory."""
+    D = 512
     widths = np.ones(D // 16, dtype=np.uint8)
     blob = calibrate.write_blob(
         [(0, 0, np.zeros(D), np.eye(D), np.ones(D), widths)], 4, 16,
         int(widths.size * calibrate.width_cost_units(1) * 16))
+    assert load_raw(kv, blob) == kv.KVTC_ENOTSUP
+    widths = np.zeros(D // 16, dtype=np.uint8)
+    widths[:25] = 2
+    blob = calibrate.write_blob(
+        [(0, 0, np.zeros(D), np.eye(D), np.ones(D), widths)], 4, 16, 2048)
     assert load_raw(kv, blob) == kv.KVTC_ENOTSUP

@@ -21,8 +21,8 @@ import pytest
 import synth
 from oracle import codec
 
-from _parity import (blob_for, calibrate_workload, check_decompress,
-                     check_records, record, stream_calibs)
+from _parity import (blob_for, calibrate_forced, calibrate_workload,
+                     check_decompress, check_records, record, stream_calibs)
 
 pytestmark = pytest.mark.gpu
 
@@ -46,7 +46,7 @@ def from_dev(t) -> np.ndarray:
     return t.cpu().numpy().view(np.uint16)
 
 
-def check_stream_records(g: bytes, x: np.ndarray, sc_enc, T, w):
+def check_stream_records(g: bytes, x: np.ndarray, sc_enc, T, w, tag=None):
     """Raw rows bit-exact and every record within the parity rule."""
     s_, w_, tc = codec.split_tokens(T, w.sink, w.window)
     raw = (s_ + w_) * w.D * 2
@@ -54,25 +54,27 @@ def check_stream_records(g: bytes, x: np.ndarray, sc_enc, T, w):
     assert g[:raw] == o_raw, "raw rows differ"
     grec = np.frombuffer(g, np.uint8, tc * sc_enc.R, raw).reshape(tc, sc_enc.R)
     st = check_records(grec, x[s_:T - w_], sc_enc)
-    record(w.name, st=st)
+    record(tag or w.name, st=st)
     assert st["bad"] == 0, st
 
 
-def check_stream_restore(got: np.ndarray, oracle_bytes: bytes, T, sc_dec, w):
+def check_stream_restore(got: np.ndarray, oracle_bytes: bytes, T, sc_dec, w,
+                         tag=None):
     s_, w_, tc = codec.split_tokens(T, w.sink, w.window)
     ref = codec.decompress_stream(oracle_bytes, T, sc_dec)
     np.testing.assert_array_equal(got[:s_], ref[:s_])
     np.testing.assert_array_equal(got[T - w_:], ref[T - w_:])
     st = check_decompress(got[s_:T - w_], ref[s_:T - w_])
-    record(w.name, dst=st)
+    record(tag or w.name, dst=st)
     assert st["ok"], st
 
 
-def run_contiguous(kv, torch, name, sample, streamed=False):
+def run_contiguous(kv, torch, name, sample, streamed=False, blob=None,
+                   tag=None):
     w = synth.WORKLOADS[name]
     streams = w.streams()
-    entries = calibrate_workload(name, streams)
-    blob = blob_for(name, entries)
+    if blob is None:
+        blob = blob_for(name, calibrate_workload(name, streams))
     scs = stream_calibs(blob)
     calib = kv.kvtc_calib_load(blob, 0)
     T, D = w.tokens, w.D
@@ -91,7 +93,7 @@ def run_contiguous(kv, torch, name, sample, streamed=False):
         sc_enc, _ = scs[(l, k)]
         x = from_dev(src[idx])
         check_stream_records(gbytes[idx * sb:(idx + 1) * sb].tobytes(), x,
-                             sc_enc, T, w)
+                             sc_enc, T, w, tag)
         o = codec.compress_stream(x, sc_enc)
         assert len(o) == sb
         dec_in[idx * sb:(idx + 1) * sb] = np.frombuffer(o, np.uint8)
@@ -114,8 +116,27 @@ def run_contiguous(kv, torch, name, sample, streamed=False):
     for idx in sample:
         l, k = streams[idx]
         check_stream_restore(from_dev(outs[idx]), oracle_bytes[idx], T,
-                             scs[(l, k)][1], w)
+                             scs[(l, k)][1], w, tag)
     calib.free()
+
+
+def test_full_llama31_8b_8k_flat_k256_sampled(kv, torch):
+    """Config-2 shape with a flat spectrum: 64 streams x 8192 tokens, the DP
+    keeps k = 256 on every stream (single-A-buffer reconstruction)."""
+    run_contiguous(kv, torch, "llama31_8b_8k_flat", (0, 1, 33, 62, 63))
+
+
+def test_full_llama31_8b_8k_k336_sampled(kv, torch):
+    """Config-2 workload with 21 one-bit groups set by hand on every stream
+    (k = 336, the most its 1024-bit budget holds): the wide projection (two
+    MMAs per K step) and reconstruction at full size."""
+    name = "llama31_8b_8k"
+    w = synth.WORKLOADS[name]
+    widths = np.zeros(w.D // 16, dtype=np.int64)
+    widths[:21] = 1
+    blob = blob_for(name, calibrate_forced(name, w.streams(), widths))
+    run_contiguous(kv, torch, name, (0, 1, 30, 63), blob=blob,
+                   tag=f"{name}, 21 one-bit groups (k = 336)")
 
 
 def test_full_mistral_nemo_12b_32k_sampled(kv, torch):

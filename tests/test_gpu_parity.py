@@ -5,8 +5,8 @@ import pytest
 import synth
 from oracle import codec, fp
 
-from _parity import (blob_for, calibrate_workload, check_decompress,
-                     check_records, record, stream_calibs)
+from _parity import (blob_for, calibrate_forced, calibrate_workload,
+                     check_decompress, check_records, record, stream_calibs)
 
 pytestmark = pytest.mark.gpu
 
@@ -39,12 +39,15 @@ def from_dev(t) -> np.ndarray:
     return t.cpu().numpy().view(np.uint16)
 
 
-def run_roundtrip(kv, torch, name, streams, T, ld_pad=0, sample=None):
+def run_roundtrip(kv, torch, name, streams, T, ld_pad=0, sample=None,
+                  blob=None, tag=None):
     """Compress x of each stream on the GPU and with the oracle, compare;
-    decompress the oracle's bitstream on the GPU, compare."""
+    decompress the oracle's bitstream on the GPU, compare.  `blob`: a
+    calibration to use instead of the oracle's DP calibration of `name`."""
     w = synth.WORKLOADS[name]
-    entries = calibrate_workload(name, streams)
-    blob = blob_for(name, entries)
+    if blob is None:
+        blob = blob_for(name, calibrate_workload(name, streams))
+    tag = tag or name
     scs = stream_calibs(blob)
     calib = kv.kvtc_calib_load(blob, 0)
     layers = sorted({l for l, _ in streams})
@@ -80,7 +83,7 @@ def run_roundtrip(kv, torch, name, streams, T, ld_pad=0, sample=None):
         rows = np.arange(tc) if sample is None else sample(tc)
         grec = np.frombuffer(g, np.uint8, tc * R, raw).reshape(tc, R)[rows]
         st = check_records(grec, xs[(l, k)][s_ + rows], sc_enc)
-        record(name, st=st)
+        record(tag, st=st)
         assert st["bad"] == 0, st
         stats.append(st)
         oracle_stream[(l, k)] = o
@@ -104,7 +107,7 @@ def run_roundtrip(kv, torch, name, streams, T, ld_pad=0, sample=None):
         np.testing.assert_array_equal(got[:s_], ref[:s_])
         np.testing.assert_array_equal(got[T - w_:], ref[T - w_:])
         st = check_decompress(got[s_:T - w_], ref[s_:T - w_])
-        record(name, dst=st)
+        record(tag, dst=st)
         assert st["ok"], st
         dstats.append(st)
         if ld_pad:  # padding columns untouched
@@ -143,6 +146,51 @@ def test_d384_128_column_chunks(kv, torch):
                   900, ld_pad=64)
 
 
+def test_flat_spectrum_k256_takes_the_single_a_buffer(kv, torch):
+    """Flat spectrum at 1 bit per coefficient: the DP keeps 16 two-bit
+    groups, k = 256.  The projection runs one N = 256 MMA per K step into
+    double-buffered accumulators; the reconstruction's A operand (k + 16 =
+    272 fp16 columns) takes the single-buffer layout and its B operand two
+    ring stages per chunk."""
+    run_roundtrip(kv, torch, "llama31_8b_8k_flat", [(0, 0), (0, 1), (1, 0)],
+                  1000)
+
+
+def forced_blob(name, streams, ngroups, budget_bits):
+    """Oracle basis of `name`'s streams with the first `ngroups` groups at
+    width 1 and the rest dropped."""
+    w = synth.WORKLOADS[name]
+    widths = np.zeros(w.D // 16, dtype=np.int64)
+    widths[:ngroups] = 1
+    return blob_for(name, calibrate_forced(name, streams, widths),
+                    budget_bits)
+
+
+@pytest.mark.parametrize("ngroups,budget", [(21, 1024), (28, 1408)])
+def test_hand_set_widths_k336_and_k448(kv, torch, ngroups, budget):
+    """k = 336 (21 one-bit groups, the most a 1024-bit budget holds) and
+    k = 448 (28 groups, 176-byte records): the projection issues two MMAs per
+    K step (N = 256 and N = k - 256) into one k-column accumulator, and the
+    reconstruction contracts k + 16 = 352 or 464 columns from the single A
+    buffer, its B operand in two ring stages per chunk."""
+    name = "llama31_8b_8k"
+    streams = [(2, 0), (2, 1), (3, 0)]
+    blob = forced_blob(name, streams, ngroups, budget)
+    run_roundtrip(kv, torch, name, streams, 2049, ld_pad=64, blob=blob,
+                  tag=f"{name}, {ngroups} one-bit groups (k = "
+                      f"{16 * ngroups})")
+
+
+def test_paged_restore_k336(kv, torch):
+    """Paged restore of the Qwen-shaped streams (D = 512, two output
+    chunks) with 21 one-bit groups: k = 336 through the block table."""
+    name = "qwen25_7b_paged"
+    streams = [(0, 0), (0, 1)]
+    blob = forced_blob(name, streams, 21, 1024)
+    run_paged(kv, torch, name, streams, [700, 37, 4096, 300], blob=blob,
+              tag=f"{name}, 21 one-bit groups (k = 336)")
+
+
 def test_llama_shape_several_streams_ragged(kv, torch):
     stats, dstats = run_roundtrip(
         kv, torch, "llama31_8b_8k", [(3, 0), (3, 1), (4, 0), (4, 1)], 1000)
@@ -171,11 +219,12 @@ def test_paged_restore_256_byte_records(kv, torch):
               [600, 21, 300])
 
 
-def run_paged(kv, torch, name, streams, Ts):
+def run_paged(kv, torch, name, streams, Ts, blob=None, tag=None):
     w = synth.WORKLOADS[name]
     nl = max(l for l, _ in streams) + 1
-    entries = calibrate_workload(name, streams)
-    blob = blob_for(name, entries)
+    if blob is None:
+        blob = blob_for(name, calibrate_workload(name, streams))
+    tag = tag or name
     scs = stream_calibs(blob)
     calib = kv.kvtc_calib_load(blob, 0)
     bs = 16
@@ -210,7 +259,7 @@ def run_paged(kv, torch, name, streams, Ts):
             np.testing.assert_array_equal(got[:s_], ref[:s_])
             np.testing.assert_array_equal(got[T - w_:], ref[T - w_:])
             st = check_decompress(got[s_:T - w_], ref[s_:T - w_])
-            record(name + " (paged)", dst=st)
+            record(tag + " (paged)", dst=st)
             assert st["ok"], st
     # untouched blocks keep their contents
     used = set(table[r, t] for r, T in enumerate(Ts)
