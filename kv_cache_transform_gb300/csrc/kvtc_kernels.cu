@@ -312,6 +312,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
   uint64_t* acc_full = a_full + 4;              // [4]
   uint64_t* acc_empty = a_full + 8;             // [4], leader's used
   uint64_t* mma_done = a_full + 12;
+  uint64_t* grp_done = a_full + 13;             // [4], per CTA
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(
       reinterpret_cast<uint8_t*>(bar) + kDecBarBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -336,9 +337,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&acc_full[i], 1);
-      // the epilogue warps of both CTAs that read a chunk arrive with
-      // counts adding up to 32 whatever the chunk width
-      mbar_init(&acc_empty[i], 32);
+      // one arrival per CTA: the epilogue warps that read a chunk meet on
+      // this CTA's grp_done barrier (arrival counts adding up to 16 whatever
+      // the chunk width) and one of them arrives for all
+      mbar_init(&acc_empty[i], 2);
+      mbar_init(&grp_done[i], 16);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -440,8 +443,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
           const uint32_t accb = chunk & nbm;
           KVTC_TR(0)
           if (!acc_ready &&
-              !mbar_wait(&acc_empty[accb], ((chunk >> lg) & 1u) ^ 1u,
-                         abort_flag)) {
+              !mbar_wait_poll(&acc_empty[accb], ((chunk >> lg) & 1u) ^ 1u,
+                              abort_flag)) {
             ok = false;
             break;
           }
@@ -450,7 +453,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
           const uint32_t c_next = chunk + 1;
           for (int h = 0; h < nbs; ++h) {
             KVTC_TR(0)
-            if (!b_ready && !mbar_wait(&full_b[s], ph, abort_flag)) {
+            if (!b_ready && !mbar_wait_poll(&full_b[s], ph, abort_flag)) {
               ok = false;
               break;
             }
@@ -517,8 +520,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
     bool ok = true;
     KVTC_TR_DECL
     for (int item = pair; item < total; item += npairs, ++it) {
-      if ((it & 1u) != set) continue;
-      // A buffers: two of 128 columns, or one of 256 (wide launch)
+      // A buffers: two of 128 columns, each filled by its own set of warps
+      // on alternate tiles; or one of 256 columns (wide launch), filled by
+      // set 0 alone, tile after tile: with two sets on one buffer a set
+      // could wait on its barriers two phases ahead, where a parity wait
+      // cannot tell the phase it wants from the one before
+      if (p.wide ? set != 0u : (it & 1u) != set) continue;
       const uint32_t abuf = p.wide ? 0u : it & 1u;
       const uint32_t ause = p.wide ? it : it >> 1;
       const DecTile t = resolve(p, item);
@@ -661,25 +668,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         }
         tc_fence_after();
         KVTC_TR(1)
-        // 64 columns as 32 bf16 pairs, packed 32 columns at a time
+        // 64 columns as 32 bf16 pairs, loaded 32 columns at a time; the
+        // accumulator is released as soon as the second load has landed,
+        // before its columns are packed
         uint32_t pk[32];
         {
           const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) +
                                  accb * (uint32_t)nc + (uint32_t)col0;
+          float v[32];
+          tmem_ld32(taddr, v);
+          tmem_wait_ld();
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            float v[32];
-            tmem_ld32(taddr + (uint32_t)hh * 32u, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[16 * hh + i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+          tmem_ld32(taddr + 32u, v);
+          tmem_wait_ld();
+          // the warps reading this accumulator arrive on this CTA's
+          // grp_done barrier; the group's first warp waits for all of them
+          // and arrives once for the CTA on the leader's acc_empty
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive_n(&grp_done[accb], 1u << lg);
+            if ((e & ((16 >> lg) - 1)) == 0) {
+              if (mbar_wait(&grp_done[accb], (chunk >> lg) & 1u, abort_flag))
+                mbar_arrive_cluster(acc_empty_leader + accb * 8u);
+              else
+                raise_abort(abort_flag, p.status);
+            }
           }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[16 + i] = pack_bf16(v[2 * i], v[2 * i + 1]);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0)
-          mbar_arrive_cluster_n(acc_empty_leader + accb * 8u, 1u << lg);
         if constexpr (!kPaged) {
           if (lane == 0) bulk_wait_read<0>();  // the last store read stg_w
         }
@@ -911,20 +933,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
           const uint64_t ad = desc_s0 + s * stage_units;
           const uint64_t bd = ad + b_units;
           const uint32_t two = kb + 1 < nkb;
+          // (the tensor pipe queues almost nothing ahead, so a tile with
+          // one MMA per K step runs without the second, predicated-off
+          // instruction between its MMAs)
+          if (n2 == 0) {
 #pragma unroll
-          for (int j = 0; j < 2; ++j)
+            for (int j = 0; j < 2; ++j)
 #pragma unroll
-            for (int st = 0; st < 4; ++st) {
-              mma_ss_pair_if(d, ad + (uint64_t)j * a_kb_units + 2u * st,
-                             bd + (uint64_t)j * b_kb_units + 2u * st, idesc,
-                             (kb | j | st) != 0, j == 0 || two);
-              // rows [128, k/2) of the half: 128 rows x 128 B further
-              mma_ss_pair_if(d + 256u,
-                             ad + (uint64_t)j * a_kb_units + 2u * st,
-                             bd + (uint64_t)j * b_kb_units + 2u * st + 1024u,
-                             idesc2, (kb | j | st) != 0,
-                             n2 != 0 && (j == 0 || two));
-            }
+              for (int st = 0; st < 4; ++st)
+                mma_ss_pair_if(d, ad + (uint64_t)j * a_kb_units + 2u * st,
+                               bd + (uint64_t)j * b_kb_units + 2u * st, idesc,
+                               (kb | j | st) != 0, j == 0 || two);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+              for (int st = 0; st < 4; ++st) {
+                mma_ss_pair_if(d, ad + (uint64_t)j * a_kb_units + 2u * st,
+                               bd + (uint64_t)j * b_kb_units + 2u * st, idesc,
+                               (kb | j | st) != 0, j == 0 || two);
+                // rows [128, k/2) of the half: 128 rows x 128 B further
+                mma_ss_pair_if(
+                    d + 256u, ad + (uint64_t)j * a_kb_units + 2u * st,
+                    bd + (uint64_t)j * b_kb_units + 2u * st + 1024u, idesc2,
+                    (kb | j | st) != 0, j == 0 || two);
+              }
+          }
           tc_commit_pair(&empty[s], 3);
           if (++s == (uint32_t)nst) {
             s = 0;

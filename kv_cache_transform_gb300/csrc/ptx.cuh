@@ -75,6 +75,14 @@ __device__ __forceinline__ void mbar_arrive_cluster_n(uint32_t cluster_addr,
                : "memory");
 }
 
+// Arrive on a barrier of this CTA with an arrival count of `n`.
+__device__ __forceinline__ void mbar_arrive_n(uint64_t* bar, uint32_t n) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "r"(n)
+               : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar,
                                                       uint32_t bytes) {
   asm volatile(
@@ -154,6 +162,20 @@ __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity,
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           const volatile int* abort_flag) {
   return mbar_wait_for(bar, parity, abort_flag, kWaitNs);
+}
+
+// Bounded wait that polls without a suspend hint: for the single MMA-issuing
+// thread, which has nothing else to do and should see a phase complete as
+// early as possible.
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity,
+                                               const volatile int* abort_flag) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitNs) return false;
+  }
 }
 
 // Same bound without the abort flag: used to let copies and MMAs that were

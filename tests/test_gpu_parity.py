@@ -152,8 +152,8 @@ def test_flat_spectrum_k256_takes_the_single_a_buffer(kv, torch):
     double-buffered accumulators; the reconstruction's A operand (k + 16 =
     272 fp16 columns) takes the single-buffer layout and its B operand two
     ring stages per chunk."""
-    run_roundtrip(kv, torch, "llama31_8b_8k_flat", [(0, 0), (0, 1), (1, 0)],
-                  1000)
+    run_roundtrip(kv, torch, "llama31_8b_8k_flat",
+                  [(0, 0), (0, 1), (1, 0), (1, 1)], 1000)
 
 
 def forced_blob(name, streams, ngroups, budget_bits):
@@ -174,7 +174,7 @@ def test_hand_set_widths_k336_and_k448(kv, torch, ngroups, budget):
     reconstruction contracts k + 16 = 352 or 464 columns from the single A
     buffer, its B operand in two ring stages per chunk."""
     name = "llama31_8b_8k"
-    streams = [(2, 0), (2, 1), (3, 0)]
+    streams = [(2, 0), (2, 1), (3, 0), (3, 1)]
     blob = forced_blob(name, streams, ngroups, budget)
     run_roundtrip(kv, torch, name, streams, 2049, ld_pad=64, blob=blob,
                   tag=f"{name}, {ngroups} one-bit groups (k = "
