@@ -272,8 +272,10 @@ int kvtc_fields_unpack(const kvtc_calib* calib, int layer0, int nlayers,
  *                 upper bound); *blob_bytes receives the size (also when
  *                 the capacity is too small: ESIZE).
  * Unlike the codec calls it allocates temporary device memory (freed before
- * returning) and synchronises cuda_stream.  fp64 arithmetic; covariance and
- * coefficient products use cuBLAS, the eigensolver cuSOLVER.
+ * returning) and synchronises cuda_stream.  fp64 arithmetic on the device:
+ * mean, covariance, eigenvector order and signs, coefficient products,
+ * distortion table and DP are this library's kernels; the symmetric
+ * eigensolver is cuSOLVER's (syevd).
  * Errors: EINVAL, ENOMEM, ECUDA, ESIZE.
  */
 int kvtc_calibrate(int cuda_device, int n, const int* layers, const int* kvs,

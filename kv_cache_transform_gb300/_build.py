@@ -16,7 +16,7 @@ FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
          "-I" + os.path.join(ROOT, "include")]
 SOURCES = ["kvtc_host.cu", "kvtc_kernels.cu", "kvtc_calib.cu",
            "kvtc_static.cu", "kvtc_fieldpack.cu"]
-LIBS = ["-lcublas", "-lcusolver"]
+LIBS = ["-lcusolver"]
 DEPS = SOURCES + ["kvtc_internal.cuh", "ptx.cuh"]
 
 

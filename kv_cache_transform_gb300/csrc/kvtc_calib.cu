@@ -4,11 +4,13 @@
 // quantiser, and the DP bit allocation under the budget.  Writes a
 // calibration blob (format in include/kvtc.h).
 //
-// Arithmetic is fp64 throughout.  The covariance and the coefficient
-// products are plain dense GEMMs (cuBLAS); the symmetric eigensolver is
-// cuSOLVER's divide-and-conquer routine.  Mean, centring, the distortion
-// table and the bit allocation are this library's own code.
-#include <cublas_v2.h>
+// Arithmetic is fp64 throughout.  Mean, centring, the covariance (Gram
+// matrix of the centred rows), the descending order and sign rule of the
+// eigenvectors, the coefficient projection, the distortion table and the
+// DP bit allocation are this library's own kernels; the symmetric
+// eigensolver is cuSOLVER's divide-and-conquer routine (a one-time
+// library step like a GEMM; a hand-written Jacobi iteration would be
+// slower at D = 1024 and is not the hot path).
 #include <cusolverDn.h>
 
 #include <algorithm>
@@ -48,6 +50,145 @@ __global__ void centre_kernel(const uint16_t* x, int64_t N, int64_t ld, int D,
   const int64_t t = i / D;
   const int d = (int)(i - t * D);
   xc[i] = bf16_to_f64(x[t * ld + d]) - mu[d];
+}
+
+// fp64 tiles of 64 x 64 outputs, 256 threads, 4 x 4 outputs per thread,
+// the contraction in steps of 16.
+constexpr int kGT = 64;
+constexpr int kGK = 16;
+
+// Covariance of the centred rows xc [N][D] (row-major): for the tile pair
+// (ti >= tj), C[i][j] = C[j][i] = alpha * sum_t xc[t][i] xc[t][j]; C is
+// D x D and symmetric, so its storage order does not matter.
+__global__ void __launch_bounds__(256) gram_kernel(const double* xc,
+                                                   int64_t N, int D,
+                                                   double alpha, double* C) {
+  const int ti = blockIdx.y, tj = blockIdx.x;
+  if (tj > ti) return;
+  __shared__ double As[kGK][kGT + 1], Bs[kGK][kGT + 1];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int i0 = ti * kGT, j0 = tj * kGT;
+  double acc[4][4] = {};
+  for (int64_t t0 = 0; t0 < N; t0 += kGK) {
+    for (int e = threadIdx.x; e < kGK * kGT; e += 256) {
+      const int tk = e / kGT, c = e - tk * kGT;
+      const int64_t t = t0 + tk;
+      As[tk][c] = (t < N && i0 + c < D) ? xc[t * D + i0 + c] : 0.0;
+      Bs[tk][c] = (t < N && j0 + c < D) ? xc[t * D + j0 + c] : 0.0;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int tk = 0; tk < kGK; ++tk) {
+      double a[4], b[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        a[r] = As[tk][ty * 4 + r];
+        b[r] = Bs[tk][tx * 4 + r];
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[r][q] = fma(a[r], b[q], acc[r][q]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = i0 + ty * 4 + r, j = j0 + tx * 4 + q;
+      if (i < D && j < D) {
+        C[(int64_t)i * D + j] = alpha * acc[r][q];
+        C[(int64_t)j * D + i] = alpha * acc[r][q];
+      }
+    }
+}
+
+// Eigenvectors in descending order of eigenvalue, each signed so that its
+// largest-magnitude entry is positive (the first such entry on ties).
+// evec: column j (contiguous, D entries) = eigenvector of the j-th smallest
+// eigenvalue w[j].  Block j writes V column j (contiguous) = the (D-1-j)-th
+// eigenvector times its sign, and ev[j] = w[D-1-j].
+__global__ void __launch_bounds__(256) order_sign_kernel(const double* evec,
+                                                         const double* w,
+                                                         int D, double* V,
+                                                         double* ev) {
+  const int j = blockIdx.x;
+  const double* src = evec + (int64_t)(D - 1 - j) * D;
+  __shared__ double sv[256];
+  __shared__ int si[256];
+  double best = -1.0;
+  int arg = D;
+  for (int d = threadIdx.x; d < D; d += 256) {
+    const double a = fabs(src[d]);
+    if (a > best) {  // d ascends within a thread: ties keep the first
+      best = a;
+      arg = d;
+    }
+  }
+  sv[threadIdx.x] = best;
+  si[threadIdx.x] = arg;
+  __syncthreads();
+  for (int s = 128; s > 0; s >>= 1) {
+    if ((int)threadIdx.x < s) {
+      const double ob = sv[threadIdx.x + s];
+      const int oi = si[threadIdx.x + s];
+      if (ob > sv[threadIdx.x] || (ob == sv[threadIdx.x] && oi < si[threadIdx.x])) {
+        sv[threadIdx.x] = ob;
+        si[threadIdx.x] = oi;
+      }
+    }
+    __syncthreads();
+  }
+  const double sgn = src[si[0]] < 0.0 ? -1.0 : 1.0;
+  for (int d = threadIdx.x; d < D; d += 256)
+    V[(int64_t)j * D + d] = sgn * src[d];
+  if (threadIdx.x == 0) ev[j] = w[D - 1 - j];
+}
+
+// Coefficients of every component: coef[t][j] = sum_d xc[t][d] V[d][j],
+// xc [N][D] row-major, V stored by columns (column j contiguous).
+__global__ void __launch_bounds__(256) project_kernel(const double* xc,
+                                                      int64_t N, int D,
+                                                      const double* V,
+                                                      double* coef) {
+  __shared__ double As[kGK][kGT + 1], Bs[kGK][kGT + 1];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int64_t r0 = (int64_t)blockIdx.y * kGT;
+  const int j0 = blockIdx.x * kGT;
+  double acc[4][4] = {};
+  for (int d0 = 0; d0 < D; d0 += kGK) {
+    for (int e = threadIdx.x; e < kGK * kGT; e += 256) {
+      const int c = e / kGK, dk = e - c * kGK;  // dk fastest: contiguous d
+      const int d = d0 + dk;
+      const int64_t t = r0 + c;
+      As[dk][c] = (t < N && d < D) ? xc[t * D + d] : 0.0;
+      Bs[dk][c] = (j0 + c < D && d < D) ? V[(int64_t)(j0 + c) * D + d] : 0.0;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int dk = 0; dk < kGK; ++dk) {
+      double a[4], b[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        a[r] = As[dk][ty * 4 + r];
+        b[r] = Bs[dk][tx * 4 + r];
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[r][q] = fma(a[r], b[q], acc[r][q]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int64_t t = r0 + ty * 4 + r;
+      const int j = j0 + tx * 4 + q;
+      if (t < N && j < D) coef[t * D + j] = acc[r][q];
+    }
 }
 
 // Directed fp64 -> fp16 roundings: fp64 -> fp32 and fp32 -> fp16 in the same
@@ -114,40 +255,63 @@ __global__ void distortion_kernel(const double* c, int64_t N, int D,
       part[((int64_t)blockIdx.x * G + g) * (kBmax + 1) + b] = red[0][b];
 }
 
-int cost_units(int b) { return b == 0 ? 0 : 2 + b; }
+// Distortion table E[g][b] = sum over the token tiles of part[tile][g][b].
+__global__ void distortion_sum_kernel(const double* part, int64_t tiles,
+                                      int G, double* E) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= G * (kBmax + 1)) return;
+  double s = 0.0;
+  for (int64_t t = 0; t < tiles; ++t) s += part[t * G * (kBmax + 1) + i];
+  E[i] = s;
+}
 
-// DP over groups: least summed distortion within budget_bits / 16 units;
-// ties keep the smaller width.
-std::vector<uint8_t> allocate(const std::vector<double>& E, int G, int bmax,
-                              int budget_bits) {
-  const int U = budget_bits / 16;
-  std::vector<double> F((size_t)(G + 1) * (U + 1), 0.0);
-  std::vector<uint8_t> choice((size_t)(G + 1) * (U + 1), 0);
-  for (int g = 1; g <= G; ++g)
-    for (int u = 0; u <= U; ++u) {
-      double best = std::numeric_limits<double>::infinity();
+__device__ __forceinline__ int cost_units(int b) { return b == 0 ? 0 : 2 + b; }
+
+// DP over groups (one block): F[g][u] = least summed distortion of the
+// first g groups within u units of 16 bits, choosing b = 0 .. bmax in
+// ascending order with strict improvement only (ties keep the smaller
+// width); then the widths by backtracking from u = U.  No allocation
+// exceeds 10 units per group, so u is capped at 10 G: for larger u every
+// F[g][u] equals F[g][10 g] and every choice equals the one there, so the
+// widths are the same as with the full budget.  F: 2 x (U + 1) doubles of
+// scratch, choice: G x (U + 1) bytes.
+__global__ void __launch_bounds__(256) dp_kernel(const double* E, int G,
+                                                 int bmax, int U, double* F,
+                                                 uint8_t* choice,
+                                                 uint8_t* widths) {
+  double* prev = F;
+  double* cur = F + (U + 1);
+  for (int u = threadIdx.x; u <= U; u += 256) prev[u] = 0.0;
+  __syncthreads();
+  for (int g = 1; g <= G; ++g) {
+    for (int u = threadIdx.x; u <= U; u += 256) {
+      double best = INFINITY;
       int bb = 0;
       for (int b = 0; b <= bmax; ++b) {
         const int cu = cost_units(b);
         if (cu > u) break;
-        const double v = F[(size_t)(g - 1) * (U + 1) + (u - cu)] +
-                         E[(size_t)(g - 1) * (kBmax + 1) + b];
+        const double v = prev[u - cu] + E[(g - 1) * (kBmax + 1) + b];
         if (v < best) {
           best = v;
           bb = b;
         }
       }
-      F[(size_t)g * (U + 1) + u] = best;
-      choice[(size_t)g * (U + 1) + u] = (uint8_t)bb;
+      cur[u] = best;
+      choice[(int64_t)(g - 1) * (U + 1) + u] = (uint8_t)bb;
     }
-  std::vector<uint8_t> w(G);
-  int u = U;
-  for (int g = G; g >= 1; --g) {
-    const int b = choice[(size_t)g * (U + 1) + u];
-    w[g - 1] = (uint8_t)b;
-    u -= cost_units(b);
+    __syncthreads();
+    double* t = prev;
+    prev = cur;
+    cur = t;
   }
-  return w;
+  if (threadIdx.x == 0) {
+    int u = U;
+    for (int g = G; g >= 1; --g) {
+      const int b = choice[(int64_t)(g - 1) * (U + 1) + u];
+      widths[g - 1] = (uint8_t)b;
+      u -= cost_units(b);
+    }
+  }
 }
 
 struct Out {
@@ -190,11 +354,14 @@ int kvtc_calibrate(int cuda_device, int n, const int* layers, const int* kvs,
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   const int G = D / kGroupC;
   const int64_t tiles = (N + kTokTile - 1) / kTokTile;
+  // DP units: the budget's, capped where no allocation reaches (10 per group)
+  const int U = std::min(budget_bits / 16, 10 * G);
 
   double *mu = nullptr, *xc = nullptr, *cov = nullptr, *w = nullptr,
-         *V = nullptr, *coef = nullptr, *part = nullptr, *work = nullptr;
+         *V = nullptr, *ev = nullptr, *coef = nullptr, *part = nullptr,
+         *E = nullptr, *F = nullptr, *work = nullptr;
+  uint8_t *choice = nullptr, *dwidths = nullptr;
   int* info = nullptr;
-  cublasHandle_t blas = nullptr;
   cusolverDnHandle_t solver = nullptr;
   int ret = KVTC_OK;
   auto cu = [&](cudaError_t e) {
@@ -210,16 +377,18 @@ int kvtc_calibrate(int cuda_device, int n, const int* layers, const int* kvs,
   do {
     if (!cu(cudaMalloc(&mu, 8LL * D)) || !cu(cudaMalloc(&xc, 8LL * N * D)) ||
         !cu(cudaMalloc(&cov, 8LL * D * D)) || !cu(cudaMalloc(&w, 8LL * D)) ||
-        !cu(cudaMalloc(&V, 8LL * D * D)) ||
+        !cu(cudaMalloc(&V, 8LL * D * D)) || !cu(cudaMalloc(&ev, 8LL * D)) ||
         !cu(cudaMalloc(&coef, 8LL * N * D)) ||
         !cu(cudaMalloc(&part, 8LL * tiles * G * (kBmax + 1))) ||
+        !cu(cudaMalloc(&E, 8LL * G * (kBmax + 1))) ||
+        !cu(cudaMalloc(&F, 16LL * (U + 1))) ||
+        !cu(cudaMalloc(&choice, (size_t)G * (U + 1))) ||
+        !cu(cudaMalloc(&dwidths, (size_t)G)) ||
         !cu(cudaMalloc(&info, sizeof(int)))) {
       ret = KVTC_ENOMEM;
       break;
     }
-    if (cublasCreate(&blas) != CUBLAS_STATUS_SUCCESS ||
-        cusolverDnCreate(&solver) != CUSOLVER_STATUS_SUCCESS ||
-        cublasSetStream(blas, st) != CUBLAS_STATUS_SUCCESS ||
+    if (cusolverDnCreate(&solver) != CUSOLVER_STATUS_SUCCESS ||
         cusolverDnSetStream(solver, st) != CUSOLVER_STATUS_SUCCESS) {
       ret = KVTC_ECUDA;
       break;
@@ -232,32 +401,43 @@ int kvtc_calibrate(int cuda_device, int n, const int* layers, const int* kvs,
       ret = ret ? ret : KVTC_ECUDA;
       break;
     }
-    std::vector<double> hcov((size_t)D * D), hw(D), hmu(D), hV((size_t)D * D);
-    std::vector<double> hpart((size_t)tiles * G * (kBmax + 1));
+    std::vector<double> hmu(D), hev(D), hV;
+    std::vector<uint8_t> widths(G);
+    const int nt = (D + kGT - 1) / kGT;
     for (int i = 0; i < n && ret == KVTC_OK; ++i) {
       const uint16_t* x = static_cast<const uint16_t*>(tokens[i]);
       column_mean_kernel<<<(D + 127) / 128, 128, 0, st>>>(x, N, ld, D, mu);
       const int64_t tot = N * D;
       centre_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(x, N, ld, D,
                                                                    mu, xc);
+      // covariance (symmetric D x D) of the centred rows
+      gram_kernel<<<dim3(nt, nt), 256, 0, st>>>(xc, N, D, 1.0 / (double)N,
+                                                cov);
       if (!cu(cudaGetLastError())) break;
-      // covariance (column-major D x D, lower triangle) of the centred rows
-      const double alpha = 1.0 / (double)N, beta = 0.0, one = 1.0;
-      if (cublasDsyrk(blas, CUBLAS_FILL_MODE_LOWER, CUBLAS_OP_N, D, (int)N,
-                      &alpha, xc, D, &beta, cov, D) != CUBLAS_STATUS_SUCCESS ||
-          cusolverDnDsyevd(solver, CUSOLVER_EIG_MODE_VECTOR,
+      if (cusolverDnDsyevd(solver, CUSOLVER_EIG_MODE_VECTOR,
                            CUBLAS_FILL_MODE_LOWER, D, cov, D, w, work, lwork,
                            info) != CUSOLVER_STATUS_SUCCESS) {
         ret = KVTC_ECUDA;
         break;
       }
+      // descending order and sign rule; coefficients of every component;
+      // distortion table; DP widths
+      order_sign_kernel<<<D, 256, 0, st>>>(cov, w, D, V, ev);
+      project_kernel<<<dim3(nt, (unsigned)((N + kGT - 1) / kGT)), 256, 0,
+                       st>>>(xc, N, D, V, coef);
+      distortion_kernel<<<dim3((unsigned)tiles, G), kTokTile, 0, st>>>(
+          coef, N, D, part);
+      distortion_sum_kernel<<<(G * (kBmax + 1) + 127) / 128, 128, 0, st>>>(
+          part, tiles, G, E);
+      dp_kernel<<<1, 256, 0, st>>>(E, G, kBmax, U, F, choice, dwidths);
       int hinfo = 0;
-      if (!cu(cudaMemcpyAsync(hcov.data(), cov, 8LL * D * D,
-                              cudaMemcpyDeviceToHost, st)) ||
-          !cu(cudaMemcpyAsync(hw.data(), w, 8LL * D, cudaMemcpyDeviceToHost,
-                              st)) ||
+      if (!cu(cudaGetLastError()) ||
           !cu(cudaMemcpyAsync(hmu.data(), mu, 8LL * D, cudaMemcpyDeviceToHost,
                               st)) ||
+          !cu(cudaMemcpyAsync(hev.data(), ev, 8LL * D, cudaMemcpyDeviceToHost,
+                              st)) ||
+          !cu(cudaMemcpyAsync(widths.data(), dwidths, (size_t)G,
+                              cudaMemcpyDeviceToHost, st)) ||
           !cu(cudaMemcpyAsync(&hinfo, info, sizeof(int),
                               cudaMemcpyDeviceToHost, st)) ||
           !cu(cudaStreamSynchronize(st)))
@@ -266,39 +446,19 @@ int kvtc_calibrate(int cuda_device, int n, const int* layers, const int* kvs,
         ret = KVTC_ECUDA;
         break;
       }
-      // descending order; sign: largest-magnitude entry positive (first on
-      // ties).  hV is column-major, column j = j-th principal vector.
-      for (int j = 0; j < D; ++j) {
-        const double* src = hcov.data() + (size_t)(D - 1 - j) * D;
-        int arg = 0;
-        for (int d = 1; d < D; ++d)
-          if (std::fabs(src[d]) > std::fabs(src[arg])) arg = d;
-        const double sgn = src[arg] < 0 ? -1.0 : 1.0;
-        for (int d = 0; d < D; ++d) hV[(size_t)j * D + d] = sgn * src[d];
-      }
-      if (!cu(cudaMemcpyAsync(V, hV.data(), 8LL * D * D,
-                              cudaMemcpyHostToDevice, st)))
-        break;
-      // coefficients, column-major D x N: coef = V^T xc
-      if (cublasDgemm(blas, CUBLAS_OP_T, CUBLAS_OP_N, D, (int)N, D, &one, V,
-                      D, xc, D, &beta, coef, D) != CUBLAS_STATUS_SUCCESS) {
-        ret = KVTC_ECUDA;
-        break;
-      }
-      distortion_kernel<<<dim3((unsigned)tiles, G), kTokTile, 0, st>>>(
-          coef, N, D, part);
-      if (!cu(cudaGetLastError()) ||
-          !cu(cudaMemcpyAsync(hpart.data(), part, 8LL * hpart.size(),
-                              cudaMemcpyDeviceToHost, st)) ||
-          !cu(cudaStreamSynchronize(st)))
-        break;
-      std::vector<double> E((size_t)G * (kBmax + 1), 0.0);
-      for (int64_t t = 0; t < tiles; ++t)
-        for (size_t j = 0; j < E.size(); ++j)
-          E[j] += hpart[(size_t)t * E.size() + j];
-      const std::vector<uint8_t> widths = allocate(E, G, kBmax, budget_bits);
+      // the kept principal vectors: per active group its 16 columns of V
       int k = 0;
       for (int g = 0; g < G; ++g) k += widths[g] ? kGroupC : 0;
+      hV.resize((size_t)k * D);
+      int a = 0;
+      for (int g = 0; g < G && ret == KVTC_OK; ++g) {
+        if (!widths[g]) continue;
+        cu(cudaMemcpyAsync(hV.data() + (size_t)a * D,
+                           V + (size_t)g * kGroupC * D, 8LL * kGroupC * D,
+                           cudaMemcpyDeviceToHost, st));
+        a += kGroupC;
+      }
+      if (!cu(cudaStreamSynchronize(st))) break;
       out.u32((uint32_t)layers[i]);
       out.u32((uint32_t)kvs[i]);
       out.u32((uint32_t)D);
@@ -307,15 +467,8 @@ int kvtc_calibrate(int cuda_device, int n, const int* layers, const int* kvs,
       std::copy(widths.begin(), widths.end(), wpad.begin());
       out.put(wpad.data(), wpad.size());
       out.put(hmu.data(), 8LL * D);
-      for (int g = 0; g < G; ++g) {
-        if (!widths[g]) continue;
-        for (int j = g * kGroupC; j < (g + 1) * kGroupC; ++j)
-          out.put(hV.data() + (size_t)j * D, 8LL * D);
-      }
-      for (int j = 0; j < D; ++j) {
-        const double ev = hw[D - 1 - j];
-        out.put(&ev, 8);
-      }
+      out.put(hV.data(), 8LL * k * D);
+      out.put(hev.data(), 8LL * D);
     }
   } while (false);
 
@@ -331,14 +484,18 @@ int kvtc_calibrate(int cuda_device, int n, const int* layers, const int* kvs,
     if (!out.ok) ret = KVTC_ESIZE;
   }
   if (solver) cusolverDnDestroy(solver);
-  if (blas) cublasDestroy(blas);
   cudaFree(mu);
   cudaFree(xc);
   cudaFree(cov);
   cudaFree(w);
   cudaFree(V);
+  cudaFree(ev);
   cudaFree(coef);
   cudaFree(part);
+  cudaFree(E);
+  cudaFree(F);
+  cudaFree(choice);
+  cudaFree(dwidths);
   cudaFree(work);
   cudaFree(info);
   if (prev >= 0) cudaSetDevice(prev);

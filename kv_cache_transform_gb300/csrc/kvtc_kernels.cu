@@ -271,26 +271,36 @@ __device__ __forceinline__ DecTile resolve(const PagedParams& p, int item) {
   return t;
 }
 
-template <class P>
-__device__ __forceinline__ char* dec_row_ptr(const P& p, const DecTile& t,
-                                             int row, int D) {
-  if constexpr (std::is_same<P, PagedParams>::value) {
-    const int tok = t.s_ + row;
-    const int bi = tok / p.block_size;
-    if (bi >= p.max_blocks) {
-      atomicOr(p.status, KVTC_FLAG_BLOCK);
-      return nullptr;
-    }
-    const int blk = p.block_table[(int64_t)t.req * p.max_blocks + bi];
-    if (blk < 0 || (int64_t)blk >= p.num_blocks) {
-      atomicOr(p.status, KVTC_FLAG_BLOCK);
-      return nullptr;
-    }
-    return t.cache +
-           ((int64_t)blk * p.block_size + tok % p.block_size) * D * 2;
-  } else {
-    return t.dst + (int64_t)row * t.ld_bytes;
+// Paged output, in two steps so that the block-table load can be issued a
+// tile before its value is needed: the entry of row `row` of tile t (or -1
+// past the table or the request's tokens), then the row's pointer in the
+// pool, or null (and KVTC_FLAG_BLOCK) when the entry is out of range.
+__device__ __forceinline__ int paged_block_load(const PagedParams& p,
+                                                const DecTile& t, int row) {
+  if (row >= t.tc) return -1;
+  const int bi = (t.s_ + row) / p.block_size;
+  if (bi >= p.max_blocks) return -2;
+  return __ldg(p.block_table + (int64_t)t.req * p.max_blocks + bi);
+}
+__device__ __forceinline__ char* paged_row_ptr(const PagedParams& p,
+                                               const DecTile& t, int row,
+                                               int D, int blk) {
+  if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+    atomicOr(p.status, KVTC_FLAG_BLOCK);
+    return nullptr;
   }
+  const int tok = t.s_ + row;
+  return t.cache +
+         ((int64_t)blk * p.block_size + tok % p.block_size) * D * 2;
+}
+__device__ __forceinline__ int paged_block_load(const DecParams&,
+                                                const DecTile&, int) {
+  return -1;
+}
+__device__ __forceinline__ char* paged_row_ptr(const DecParams&,
+                                               const DecTile&, int, int,
+                                               int) {
+  return nullptr;
 }
 
 template <class P>
@@ -312,7 +322,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
   uint64_t* acc_full = a_full + 4;              // [4]
   uint64_t* acc_empty = a_full + 8;             // [4], leader's used
   uint64_t* mma_done = a_full + 12;
-  uint64_t* grp_done = a_full + 13;             // [4], per CTA
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(
       reinterpret_cast<uint8_t*>(bar) + kDecBarBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -337,11 +346,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&acc_full[i], 1);
-      // one arrival per CTA: the epilogue warps that read a chunk meet on
-      // this CTA's grp_done barrier (arrival counts adding up to 16 whatever
-      // the chunk width) and one of them arrives for all
-      mbar_init(&acc_empty[i], 2);
-      mbar_init(&grp_done[i], 16);
+      // the epilogue warps of both CTAs that read a chunk arrive with
+      // counts adding up to 32 whatever the chunk width
+      mbar_init(&acc_empty[i], 32);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -642,6 +649,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
     const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
     uint32_t chunk = 0;
     bool ok = true;
+    // paged: block-table entry of this lane's row in the next tile
+    int blk_next = -1;
+    if constexpr (kPaged) {
+      if (pair < total) {
+        const DecTile t0 = resolve(p, pair);
+        blk_next = paged_block_load(
+            p, t0, t0.tile * kPairM + (int)rank * kTileM + q * 32 + lane);
+      }
+    }
     KVTC_TR_DECL
     for (int item = pair; item < total && ok; item += npairs) {
       const DecTile t = resolve(p, item);
@@ -656,7 +672,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       const int row = wrow0 + lane;
       char* rowp = nullptr;
       if constexpr (kPaged) {
-        if (row < t.tc) rowp = dec_row_ptr(p, t, row, D);
+        // this lane's block-table entry was loaded a tile ahead (its
+        // latency under the restore's write traffic is microseconds); the
+        // next tile's is loaded now
+        if (row < t.tc) rowp = paged_row_ptr(p, t, row, D, blk_next);
+        const int nitem = item + npairs;
+        blk_next = -1;
+        if (nitem < total) {
+          const DecTile tn = resolve(p, nitem);
+          const int nrow =
+              tn.tile * kPairM + (int)rank * kTileM + q * 32 + lane;
+          blk_next = paged_block_load(p, tn, nrow);
+        }
       }
       for (int ch = 0; ch < nch; ++ch, ++chunk) {
         const uint32_t accb = chunk & nbm;
@@ -683,21 +710,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
             pk[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
           tmem_ld32(taddr + 32u, v);
           tmem_wait_ld();
-          // the warps reading this accumulator arrive on this CTA's
-          // grp_done barrier; the group's first warp waits for all of them
-          // and arrives once for the CTA on the leader's acc_empty
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive_n(&grp_done[accb], 1u << lg);
-            if ((e & ((16 >> lg) - 1)) == 0) {
-              if (mbar_wait(&grp_done[accb], (chunk >> lg) & 1u, abort_flag))
-                mbar_arrive_cluster(acc_empty_leader + accb * 8u);
-              else
-                raise_abort(abort_flag, p.status);
-            }
-          }
-          __syncwarp();
+          if (lane == 0)
+            mbar_arrive_cluster_n(acc_empty_leader + accb * 8u, 1u << lg);
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             pk[16 + i] = pack_bf16(v[2 * i], v[2 * i + 1]);

@@ -75,14 +75,6 @@ __device__ __forceinline__ void mbar_arrive_cluster_n(uint32_t cluster_addr,
                : "memory");
 }
 
-// Arrive on a barrier of this CTA with an arrival count of `n`.
-__device__ __forceinline__ void mbar_arrive_n(uint64_t* bar, uint32_t n) {
-  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
-                   smem_u32(bar)),
-               "r"(n)
-               : "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar,
                                                       uint32_t bytes) {
   asm volatile(

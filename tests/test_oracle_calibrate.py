@@ -166,3 +166,25 @@ def test_distortion_table_equals_codec_error_at_every_width(tiny, b):
     # a wider code never does worse on the same group
     if b > 1:
         assert np.all(E[:, b] <= E[:, b - 1] * (1 + 1e-12))
+
+
+def test_dp_units_beyond_ten_per_group_change_nothing():
+    """No group costs more than 10 units (two fp16 fields plus 8 planes of
+    16 bits), so the widths the DP picks with U units equal those with
+    min(U, 10 G) units, ties included: the library's device DP caps its
+    table there."""
+    rng = np.random.default_rng(0)
+    for trial in range(200):
+        G = int(rng.integers(1, 9))
+        if trial % 2:
+            E = rng.uniform(0, 1, (G, 9))
+        else:
+            E = np.sort(rng.exponential(1, (G, 9)), axis=1)[:, ::-1].copy()
+        if trial % 5 == 0:
+            E[:, 3:] = E[:, 3:4]     # equal errors above width 3: ties
+        for budget in (int(rng.integers(0, 16 * 12 * G)), 16 * 10 * G + 7,
+                       16 * 40 * G, 1 << 16):
+            full = calibrate.allocate_bits(E, budget)
+            capped = calibrate.allocate_bits(E, 16 * min(budget // 16,
+                                                         10 * G))
+            assert np.array_equal(full, capped)
