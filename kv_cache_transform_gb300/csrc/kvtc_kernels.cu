@@ -271,10 +271,9 @@ __device__ __forceinline__ DecTile resolve(const PagedParams& p, int item) {
   return t;
 }
 
-// Paged output, in two steps so that the block-table load can be issued a
-// tile before its value is needed: the entry of row `row` of tile t (or -1
-// past the table or the request's tokens), then the row's pointer in the
-// pool, or null (and KVTC_FLAG_BLOCK) when the entry is out of range.
+// Paged output: the block-table entry of row `row` of tile t (or -2 past
+// the table), then the row's pointer in the pool, or null (and
+// KVTC_FLAG_BLOCK) when the entry is out of range.
 __device__ __forceinline__ int paged_block_load(const PagedParams& p,
                                                 const DecTile& t, int row) {
   if (row >= t.tc) return -1;
@@ -303,7 +302,11 @@ __device__ __forceinline__ char* paged_row_ptr(const DecParams&,
   return nullptr;
 }
 
-template <class P>
+// kWide: a launch holding a stream with k > 240 (one 256-column A buffer,
+// and B stages of up to two per chunk); otherwise the double-buffered
+// layout with one B stage per chunk.  A template parameter, so that the
+// narrow kernels carry none of the wide layout's state.
+template <class P, bool kWide>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
     decompress_kernel(const __grid_constant__ P p) {
   extern __shared__ uint8_t smem_raw[];
@@ -375,7 +378,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         const DecTile t = resolve(p, item);
         const DevStream* ds = p.streams + t.cs;
         const int nc = ds->nc, nch = ds->D / nc, half = nc >> 1;
-        const int kbs = ds->kbs, nbs = ds->nbs;
+        const int kbs = ds->kbs, nbs = kWide ? ds->nbs : 1;
         // both halves of the chunk, kbs K blocks (a box past the last K
         // block is filled with zeros and still counts its full bytes)
         const uint32_t bytes_pair = (uint32_t)nc * 128u * (uint32_t)kbs;
@@ -425,6 +428,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       const uint64_t desc_b0 = sw128_desc(smem_u32(sB));
       for (int item = pair; item < total && ok; item += npairs) {
         const DecTile t = resolve(p, item);
+        KVTC_TR(7)
         const DevStream* ds = p.streams + t.cs;
         const int nc = ds->nc, nch = ds->D / nc;
         // 256 / nc accumulators of nc columns: log2 of their count
@@ -433,11 +437,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         const int ksteps = ds->kp / kGroup;  // kept groups + the mean step
         const int kb_units = (ds->nc / 2) * 128 / 16;  // one K block, >> 4
         const int sstep = 4 * ds->kbs;       // K steps per B stage
-        const int nbs = ds->nbs;
+        const int nbs = kWide ? ds->nbs : 1;
         const uint32_t idesc = make_idesc(256, (uint32_t)nc, 0);
         // A buffers: two of 128 columns, or one of 256 (wide launch)
-        const uint32_t abuf = p.wide ? 0u : it & 1u;
-        const uint32_t ause = p.wide ? it : it >> 1;
+        const uint32_t abuf = kWide ? 0u : it & 1u;
+        const uint32_t ause = kWide ? it : it >> 1;
         KVTC_TR(0)
         if (!mbar_wait(&a_full[abuf], ause & 1u, abort_flag)) {
           ok = false;
@@ -450,8 +454,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
           const uint32_t accb = chunk & nbm;
           KVTC_TR(0)
           if (!acc_ready &&
-              !mbar_wait_poll(&acc_empty[accb], ((chunk >> lg) & 1u) ^ 1u,
-                              abort_flag)) {
+              !mbar_wait(&acc_empty[accb], ((chunk >> lg) & 1u) ^ 1u,
+                         abort_flag)) {
             ok = false;
             break;
           }
@@ -460,7 +464,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
           const uint32_t c_next = chunk + 1;
           for (int h = 0; h < nbs; ++h) {
             KVTC_TR(0)
-            if (!b_ready && !mbar_wait_poll(&full_b[s], ph, abort_flag)) {
+            if (!b_ready && !mbar_wait(&full_b[s], ph, abort_flag)) {
               ok = false;
               break;
             }
@@ -502,10 +506,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
           }
           if (!ok) break;
           tc_commit_pair(&acc_full[accb], 3);
+          KVTC_TR(5)
           ++chunk;
         }
         if (!ok) break;
         tc_commit_pair(&a_empty[abuf], 3);
+        KVTC_TR(6)
         ++it;
       }
       KVTC_TR(0)
@@ -532,9 +538,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       // set 0 alone, tile after tile: with two sets on one buffer a set
       // could wait on its barriers two phases ahead, where a parity wait
       // cannot tell the phase it wants from the one before
-      if (p.wide ? set != 0u : (it & 1u) != set) continue;
-      const uint32_t abuf = p.wide ? 0u : it & 1u;
-      const uint32_t ause = p.wide ? it : it >> 1;
+      if (kWide ? set != 0u : (it & 1u) != set) continue;
+      const uint32_t abuf = kWide ? 0u : it & 1u;
+      const uint32_t ause = kWide ? it : it >> 1;
       const DecTile t = resolve(p, item);
       const DevStream* ds = p.streams + t.cs;
       const int R = ds->R, Ga = ds->Ga;
@@ -649,15 +655,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
     const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
     uint32_t chunk = 0;
     bool ok = true;
-    // paged: block-table entry of this lane's row in the next tile
-    int blk_next = -1;
-    if constexpr (kPaged) {
-      if (pair < total) {
-        const DecTile t0 = resolve(p, pair);
-        blk_next = paged_block_load(
-            p, t0, t0.tile * kPairM + (int)rank * kTileM + q * 32 + lane);
-      }
-    }
     KVTC_TR_DECL
     for (int item = pair; item < total && ok; item += npairs) {
       const DecTile t = resolve(p, item);
@@ -672,18 +669,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       const int row = wrow0 + lane;
       char* rowp = nullptr;
       if constexpr (kPaged) {
-        // this lane's block-table entry was loaded a tile ahead (its
-        // latency under the restore's write traffic is microseconds); the
-        // next tile's is loaded now
-        if (row < t.tc) rowp = paged_row_ptr(p, t, row, D, blk_next);
-        const int nitem = item + npairs;
-        blk_next = -1;
-        if (nitem < total) {
-          const DecTile tn = resolve(p, nitem);
-          const int nrow =
-              tn.tile * kPairM + (int)rank * kTileM + q * 32 + lane;
-          blk_next = paged_block_load(p, tn, nrow);
-        }
+        if (row < t.tc)
+          rowp = paged_row_ptr(p, t, row, D, paged_block_load(p, t, row));
       }
       for (int ch = 0; ch < nch; ++ch, ++chunk) {
         const uint32_t accb = chunk & nbm;
@@ -695,33 +682,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         }
         tc_fence_after();
         KVTC_TR(1)
-        // 64 columns as 32 bf16 pairs, loaded 32 columns at a time; the
-        // accumulator is released as soon as the second load has landed,
-        // before its columns are packed
+        // 64 columns as 32 bf16 pairs, packed 32 columns at a time
         uint32_t pk[32];
         {
           const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) +
                                  accb * (uint32_t)nc + (uint32_t)col0;
-          float v[32];
-          tmem_ld32(taddr, v);
-          tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
-          tmem_ld32(taddr + 32u, v);
-          tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0)
-            mbar_arrive_cluster_n(acc_empty_leader + accb * 8u, 1u << lg);
+          for (int hh = 0; hh < 2; ++hh) {
+            float v[32];
+            tmem_ld32(taddr + (uint32_t)hh * 32u, v);
+            tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[16 + i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+            for (int i = 0; i < 16; ++i)
+              pk[16 * hh + i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+          }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+          mbar_arrive_cluster_n(acc_empty_leader + accb * 8u, 1u << lg);
+        KVTC_TR(4)
         if constexpr (!kPaged) {
           if (lane == 0) bulk_wait_read<0>();  // the last store read stg_w
         }
         __syncwarp();
+        KVTC_TR(5)
         const uint32_t srow = smem_u32(stg_w) + lane * 128;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
@@ -1323,10 +1308,9 @@ int max_pairs_compress(int smem_bytes) {
 }
 
 int max_pairs_decompress(int smem_bytes) {
-  allow_smem((const void*)decompress_kernel<DecParams>, 232448);
-  allow_smem((const void*)decompress_kernel<PagedParams>, 232448);
-  return max_pairs((const void*)decompress_kernel<DecParams>, kDecThreads,
-                   smem_bytes);
+  allow_smem((const void*)decompress_kernel<DecParams, false>, 232448);
+  return max_pairs((const void*)decompress_kernel<DecParams, false>,
+                   kDecThreads, smem_bytes);
 }
 
 cudaError_t launch_compress(const CompParams& p, int pairs, cudaStream_t st) {
@@ -1337,14 +1321,20 @@ cudaError_t launch_compress(const CompParams& p, int pairs, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <class P>
-static cudaError_t launch_dec(const P& p, int pairs, cudaStream_t st) {
-  allow_smem((const void*)decompress_kernel<P>, 232448);
-  decompress_kernel<P><<<2 * pairs, kDecThreads,
-                         decompress_smem_bytes(p.nstages, p.rec_words), st>>>(
-      p);
+template <class P, bool kWide>
+static cudaError_t launch_dec_as(const P& p, int pairs, cudaStream_t st) {
+  allow_smem((const void*)decompress_kernel<P, kWide>, 232448);
+  decompress_kernel<P, kWide>
+      <<<2 * pairs, kDecThreads, decompress_smem_bytes(p.nstages, p.rec_words),
+         st>>>(p);
   count_launch();
   return cudaGetLastError();
+}
+
+template <class P>
+static cudaError_t launch_dec(const P& p, int pairs, cudaStream_t st) {
+  return p.wide ? launch_dec_as<P, true>(p, pairs, st)
+                : launch_dec_as<P, false>(p, pairs, st);
 }
 
 cudaError_t launch_decompress(const DecParams& p, int pairs, cudaStream_t st) {

@@ -156,20 +156,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   return mbar_wait_for(bar, parity, abort_flag, kWaitNs);
 }
 
-// Bounded wait that polls without a suspend hint: for the single MMA-issuing
-// thread, which has nothing else to do and should see a phase complete as
-// early as possible.
-__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity,
-                                               const volatile int* abort_flag) {
-  if (mbar_test_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitNs) return false;
-  }
-}
-
 // Same bound without the abort flag: used to let copies and MMAs that were
 // already issued land before the CTA exits.
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
