@@ -172,6 +172,22 @@ bool encode_store_2d(CUtensorMap* m, const void* base, uint64_t cols,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A paged pool bf16 [num_blocks][16][D] as {D, 16, num_blocks}: box {64,
+// 16, 1} is one block's rows of a 64-column slab, 128-byte swizzle.
+bool encode_pool_3d(CUtensorMap* m, const void* base, uint64_t D,
+                    uint64_t num_blocks) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {D, 16, num_blocks};
+  cuuint64_t strides[2] = {D * 2, D * 2 * 16};
+  cuuint32_t box[3] = {64u, 16u, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct DeviceGuard {
   int prev = -1;
   bool ok = true;
@@ -897,7 +913,6 @@ int kvtc_decompress_paged(const kvtc_calib* c, int layer0, int nlayers,
   int st = select_streams(c, layer0, nlayers, kv_mask, &cs, &slot);
   if (st != KVTC_OK) return st;
   if (cs.empty() || R == 0) return KVTC_OK;
-  if ((int)cs.size() > kPagedMaxStream) return KVTC_ENOTSUP;
   const int D = c->hs[cs[0]].D;
   for (size_t i = 0; i < cs.size(); ++i) {
     if (c->hs[cs[i]].D != D) return KVTC_ENOTSUP;
@@ -922,60 +937,70 @@ int kvtc_decompress_paged(const kvtc_calib* c, int layer0, int nlayers,
   if (!p) return KVTC_ENOMEM;
   const HostStream& h0 = c->hs[cs[0]];
   int ret = KVTC_OK;
-  for (int r0 = 0; r0 < R && ret == KVTC_OK; r0 += kPagedMaxReq) {
-    const int r1 = std::min(R, r0 + kPagedMaxReq);
-    std::memset(p, 0, sizeof(*p));
-    int tiles = 0;
-    int64_t raw_chunks = 0;
-    const int cpr = 2 * D / 16;
-    for (int r = r0; r < r1; ++r) {
-      int64_t s_, w_, tc;
-      split_tokens(T[r], c->sink, c->window, &s_, &w_, &tc);
-      const int i = r - r0;
-      p->src[i] = static_cast<const uint8_t*>(in[r]);
-      p->sbytes[i] = stream_bytes_of(c, h0, T[r]);
-      p->tc[i] = (int32_t)tc;
-      p->s_[i] = (int32_t)s_;
-      p->raw_rows[i] = (int32_t)(s_ + w_);
-      p->tile_begin[i] = tiles;
-      p->raw_begin[i] = raw_chunks;
-      p->req_index[i] = r;
-      tiles += (int)cs.size() * (int)((tc + kPairM - 1) / kPairM);
-      raw_chunks += (int64_t)cs.size() * (s_ + w_) * cpr;
+  // launches over groups of up to kPagedMaxReq requests and kPagedMaxStream
+  // streams (each stream of a group has its own pool tensor map)
+  for (size_t j0 = 0; j0 < cs.size() && ret == KVTC_OK; j0 += kPagedMaxStream) {
+    const size_t j1 = std::min(cs.size(), j0 + (size_t)kPagedMaxStream);
+    const int ns = (int)(j1 - j0);
+    for (int r0 = 0; r0 < R && ret == KVTC_OK; r0 += kPagedMaxReq) {
+      const int r1 = std::min(R, r0 + kPagedMaxReq);
+      std::memset(p, 0, sizeof(*p));
+      int tiles = 0;
+      int64_t raw_chunks = 0;
+      const int cpr = 2 * D / 16;
+      for (int r = r0; r < r1; ++r) {
+        int64_t s_, w_, tc;
+        split_tokens(T[r], c->sink, c->window, &s_, &w_, &tc);
+        const int i = r - r0;
+        p->src[i] = static_cast<const uint8_t*>(in[r]);
+        p->sbytes[i] = stream_bytes_of(c, h0, T[r]);
+        p->tc[i] = (int32_t)tc;
+        p->s_[i] = (int32_t)s_;
+        p->raw_rows[i] = (int32_t)(s_ + w_);
+        p->tile_begin[i] = tiles;
+        p->raw_begin[i] = raw_chunks;
+        p->req_index[i] = r;
+        tiles += ns * paged_tiles((int)s_, (int)tc);
+        raw_chunks += (int64_t)ns * (s_ + w_) * cpr;
+      }
+      p->tile_begin[r1 - r0] = tiles;
+      p->raw_begin[r1 - r0] = raw_chunks;
+      int rmax = 0, kmax = 0;
+      for (size_t j = j0; j < j1; ++j) {
+        const int jl = (int)(j - j0);
+        p->cache[jl] = static_cast<char*>(cache[slot[j]]);
+        p->cs[jl] = cs[j];
+        p->sidx[jl] = (int32_t)j;
+        rmax = std::max(rmax, c->hs[cs[j]].R);
+        kmax = std::max(kmax, c->hs[cs[j]].k);
+        if (!encode_pool_3d(&p->tm_cache[jl], cache[slot[j]], (uint64_t)D,
+                            (uint64_t)num_blocks))
+          ret = KVTC_ECUDA;
+      }
+      if (ret != KVTC_OK) break;
+      p->streams = c->d_streams;
+      p->status = c->d_status;
+      p->block_table = block_table;
+      p->num_blocks = num_blocks;
+      p->max_blocks = max_blocks;
+      p->block_size = block_size;
+      p->nreq = r1 - r0;
+      p->nstream = ns;
+      p->total_tiles = tiles;
+      p->D = D;
+      p->total_raw_chunks = raw_chunks;
+      p->rec_words = rmax / 4;
+      p->wide = kmax > kNarrowK;
+      p->nstages = decompress_stages(p->rec_words);
+      if (launch_paged_raw(*p, stream) != cudaSuccess) ret = KVTC_ECUDA;
+      const int mp =
+          max_pairs_decompress(decompress_smem_bytes(p->nstages, p->rec_words));
+      if (ret == KVTC_OK && tiles &&
+          (mp < 1 ||
+           launch_decompress_paged(*p, pairs_for(mp, tiles), stream) !=
+               cudaSuccess))
+        ret = KVTC_ECUDA;
     }
-    p->tile_begin[r1 - r0] = tiles;
-    p->raw_begin[r1 - r0] = raw_chunks;
-    for (size_t j = 0; j < cs.size(); ++j) {
-      p->cache[j] = static_cast<char*>(cache[slot[j]]);
-      p->cs[j] = cs[j];
-    }
-    p->streams = c->d_streams;
-    p->status = c->d_status;
-    p->block_table = block_table;
-    p->num_blocks = num_blocks;
-    p->max_blocks = max_blocks;
-    p->block_size = block_size;
-    p->nreq = r1 - r0;
-    p->nstream = (int)cs.size();
-    p->total_tiles = tiles;
-    p->D = D;
-    p->total_raw_chunks = raw_chunks;
-    int rmax = 0, kmax = 0;
-    for (size_t j = 0; j < cs.size(); ++j) {
-      rmax = std::max(rmax, c->hs[cs[j]].R);
-      kmax = std::max(kmax, c->hs[cs[j]].k);
-    }
-    p->rec_words = rmax / 4;
-    p->wide = kmax > kNarrowK;
-    p->nstages = decompress_stages(p->rec_words);
-    if (launch_paged_raw(*p, stream) != cudaSuccess) ret = KVTC_ECUDA;
-    const int mp =
-        max_pairs_decompress(decompress_smem_bytes(p->nstages, p->rec_words));
-    if (ret == KVTC_OK && tiles &&
-        (mp < 1 ||
-         launch_decompress_paged(*p, pairs_for(mp, tiles), stream) !=
-             cudaSuccess))
-      ret = KVTC_ECUDA;
   }
   delete p;
   return ret;

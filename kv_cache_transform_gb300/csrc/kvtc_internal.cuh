@@ -114,10 +114,21 @@ struct DecParams {
 static_assert(3 * kCompMaxSeg <= kRawListMax, "raw list too short");
 static_assert(2 * kDecMaxSeg <= kRawListMax, "raw list too short");
 
-// Paged restore: work items are (request, stream, tile).
+// Paged restore: work items are (request, stream, tile).  A request's
+// tiles cover its tokens from token 0 (not from the first coded token), so
+// that each epilogue warp's 32 rows are two whole 16-token blocks; rows
+// without a record (sink, window, past the coded range) are decoded as
+// zeros and never stored.
 constexpr int kPagedMaxReq = 256;
-constexpr int kPagedMaxStream = 256;
+constexpr int kPagedMaxStream = 64;      // streams per launch
+// Super-tiles of one (request, stream): its tokens from 0 to the last one
+// with a record, 256 at a time (none when no token is coded).
+__host__ __device__ __forceinline__ int paged_tiles(int s_, int tc) {
+  return tc > 0 ? (s_ + tc + kPairM - 1) / kPairM : 0;
+}
 struct PagedParams {
+  CUtensorMap tm_cache[kPagedMaxStream]; // pool of stream j as {D, 16,
+                                         // num_blocks}, box {64, 16, 1}
   const uint8_t* src[kPagedMaxReq];      // request's concatenated streams
   int64_t sbytes[kPagedMaxReq];          // bytes of one stream of request r
   int32_t tc[kPagedMaxReq];              // compressed tokens of request r
@@ -128,6 +139,8 @@ struct PagedParams {
   int32_t req_index[kPagedMaxReq];       // absolute request id (block table row)
   char* cache[kPagedMaxStream];          // pool of stream j
   int32_t cs[kPagedMaxStream];           // calibration stream of stream j
+  int32_t sidx[kPagedMaxStream];         // stream j's place in a request's
+                                         // concatenated streams
   const DevStream* streams;
   unsigned* status;
   const int32_t* block_table;

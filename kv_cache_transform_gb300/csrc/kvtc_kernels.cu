@@ -151,6 +151,16 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t x,
       : "memory");
 }
 
+__device__ __forceinline__ void tma_store_3d(const void* tmap, int32_t x,
+                                             int32_t y, int32_t z,
+                                             const void* ssrc) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, "
+      "%3}], [%4];" ::"l"(tmap),
+      "r"(x), "r"(y), "r"(z), "r"(smem_u32(ssrc))
+      : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -226,8 +236,10 @@ struct DecTile {
   int64_t ld_bytes;
   char* cache;         // paged: pool of this stream
   int tc, tile, cs, s_, req;
-  int seg;             // contiguous: segment (output tensor map) index
+  int seg;             // output tensor map: contiguous segment, or paged
+                       // stream of the launch
 };
+
 
 __device__ __forceinline__ DecTile resolve(const DecParams& p, int item) {
   const int lo = item / p.tiles_per_seg;
@@ -253,53 +265,22 @@ __device__ __forceinline__ DecTile resolve(const PagedParams& p, int item) {
     if (p.tile_begin[mid] <= item) lo = mid; else hi = mid - 1;
   }
   const int r = lo;
-  const int tiles = max(1, (p.tc[r] + kPairM - 1) / kPairM);
+  const int tiles = max(1, paged_tiles(p.s_[r], p.tc[r]));
   const int idx = item - p.tile_begin[r];
   const int j = idx / tiles;
   DecTile t;
   t.tile = idx - j * tiles;
   t.cs = p.cs[j];
   t.tc = p.tc[r];
-  t.rec = p.src[r] + (int64_t)j * p.sbytes[r] +
+  t.rec = p.src[r] + (int64_t)p.sidx[j] * p.sbytes[r] +
           (int64_t)p.raw_rows[r] * p.D * 2;
   t.dst = nullptr;
   t.ld_bytes = 0;
   t.cache = p.cache[j];
   t.s_ = p.s_[r];
   t.req = p.req_index[r];
-  t.seg = -1;
+  t.seg = j;
   return t;
-}
-
-// Paged output: the block-table entry of row `row` of tile t (or -2 past
-// the table), then the row's pointer in the pool, or null (and
-// KVTC_FLAG_BLOCK) when the entry is out of range.
-__device__ __forceinline__ int paged_block_load(const PagedParams& p,
-                                                const DecTile& t, int row) {
-  if (row >= t.tc) return -1;
-  const int bi = (t.s_ + row) / p.block_size;
-  if (bi >= p.max_blocks) return -2;
-  return __ldg(p.block_table + (int64_t)t.req * p.max_blocks + bi);
-}
-__device__ __forceinline__ char* paged_row_ptr(const PagedParams& p,
-                                               const DecTile& t, int row,
-                                               int D, int blk) {
-  if (blk < 0 || (int64_t)blk >= p.num_blocks) {
-    atomicOr(p.status, KVTC_FLAG_BLOCK);
-    return nullptr;
-  }
-  const int tok = t.s_ + row;
-  return t.cache +
-         ((int64_t)blk * p.block_size + tok % p.block_size) * D * 2;
-}
-__device__ __forceinline__ int paged_block_load(const DecParams&,
-                                                const DecTile&, int) {
-  return -1;
-}
-__device__ __forceinline__ char* paged_row_ptr(const DecParams&,
-                                               const DecTile&, int, int,
-                                               int) {
-  return nullptr;
 }
 
 // kWide: a launch holding a stream with k > 240 (one 256-column A buffer,
@@ -549,8 +530,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       const int my_b = lane < Ga ? (int)ds->bits[lane] : 0;
       const int my_po = lane < Ga ? (int)ds->poff[lane] : 0;
       const int row0 = t.tile * kPairM + (int)rank * kTileM + q * 32;
-      const int nvalid = min(max(t.tc - row0, 0), 32);
-      const uint8_t* rbase = t.rec + (int64_t)row0 * R;
+      // record index of the warp's first row: rows are tokens for paged
+      // output (its tiles start at token 0), records otherwise; lanes
+      // [lo, hi) have a record, the others decode zeros
+      const int rec0 =
+          std::is_same<P, PagedParams>::value ? row0 - t.s_ : row0;
+      const int lo = max(-rec0, 0);
+      const int hi = min(max(t.tc - rec0, 0), 32);
+      const uint8_t* rbase = t.rec + (int64_t)rec0 * R;
       // Coalesced 16-byte loads of the warp's 32 records (up to eight in
       // flight per lane), stored word-transposed ([word][token], row pitch
       // 33) in shared memory; done before waiting for the A buffer so the
@@ -562,7 +549,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         for (int u = 0; u < 8; ++u) {
           const int o = (b0 + u) * 512 + lane * 16;
           v[u] = make_uint4(0u, 0u, 0u, 0u);
-          if (b0 + u < nld && o / R < nvalid) v[u] = ld_nc_v4(rbase + o);
+          if (b0 + u < nld && o / R >= lo && o / R < hi)
+            v[u] = ld_nc_v4(rbase + o);
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -666,11 +654,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       const uint32_t grp = (uint32_t)e >> (4 - lg);
       const int col0 = ((e & ((16 >> lg) - 1)) >> 2) * 64;
       const int wrow0 = t.tile * kPairM + (int)rank * kTileM + q * 32;
-      const int row = wrow0 + lane;
+      // Paged: rows are tokens, and the warp's 32 are the 16-token blocks
+      // wrow0 / 16 and the one after.  A block whose 16 tokens all have
+      // records goes out as one TMA tensor store (full0 / full1); the
+      // rows of a block that also holds sink, window or no tokens go out
+      // one by one (rowp non-null for this lane's row).
+      int blk0 = -1, blk1 = -1;
+      bool full0 = false, full1 = false, any_rows = false;
       char* rowp = nullptr;
       if constexpr (kPaged) {
-        if (row < t.tc)
-          rowp = paged_row_ptr(p, t, row, D, paged_block_load(p, t, row));
+        const int c_lo = t.s_, c_hi = t.s_ + t.tc;  // tokens with records
+        int id = -1;
+        if (lane < 2) {
+          const int bi = wrow0 / 16 + lane;
+          if (bi * 16 + 16 > c_lo && bi * 16 < c_hi) {  // holds coded rows
+            id = bi < p.max_blocks
+                     ? __ldg(p.block_table + (int64_t)t.req * p.max_blocks + bi)
+                     : -1;
+            if (id < 0 || (int64_t)id >= p.num_blocks) {
+              atomicOr(p.status, KVTC_FLAG_BLOCK);
+              id = -1;
+            }
+          }
+        }
+        blk0 = __shfl_sync(0xFFFFFFFFu, id, 0);
+        blk1 = __shfl_sync(0xFFFFFFFFu, id, 1);
+        full0 = blk0 >= 0 && wrow0 >= c_lo && wrow0 + 16 <= c_hi;
+        full1 = blk1 >= 0 && wrow0 + 16 >= c_lo && wrow0 + 32 <= c_hi;
+        const int tok = wrow0 + lane;
+        const int myblk = lane < 16 ? blk0 : blk1;
+        const bool myfull = lane < 16 ? full0 : full1;
+        if (!myfull && myblk >= 0 && tok >= c_lo && tok < c_hi)
+          rowp = t.cache + ((int64_t)myblk * 16 + (tok & 15)) * D * 2;
+        any_rows = __any_sync(0xFFFFFFFFu, rowp != nullptr);
       }
       for (int ch = 0; ch < nch; ++ch, ++chunk) {
         const uint32_t accb = chunk & nbm;
@@ -702,9 +718,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         if (lane == 0)
           mbar_arrive_cluster_n(acc_empty_leader + accb * 8u, 1u << lg);
         KVTC_TR(4)
-        if constexpr (!kPaged) {
-          if (lane == 0) bulk_wait_read<0>();  // the last store read stg_w
-        }
+        if (lane == 0) bulk_wait_read<0>();  // the last store read stg_w
         __syncwarp();
         KVTC_TR(5)
         const uint32_t srow = smem_u32(stg_w) + lane * 128;
@@ -722,27 +736,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
             bulk_commit();
           }
         } else {
+          fence_proxy_async_smem();
           __syncwarp();
-          // 8 lanes per 128-byte row, four rows per store instruction
-          for (int r0 = 0; r0 < 32; r0 += 4) {
-            const int r = r0 + (lane >> 3);
-            const int sub = lane & 7;
-            char* rp = reinterpret_cast<char*>(__shfl_sync(
-                0xFFFFFFFFu, reinterpret_cast<uintptr_t>(rowp), r));
-            const uint4 val = *reinterpret_cast<const uint4*>(
-                stg_w + r * 128 + ((sub ^ (r & 7)) << 4));
-            if (rp)
-              *reinterpret_cast<uint4*>(rp + (int64_t)(ch * nc + col0) * 2 +
-                                        sub * 16) = val;
+          if (lane == 0) {
+            // whole blocks: rows 0-15 and 16-31 of the box are the two
+            // blocks (the 128-byte swizzle repeats every 8 rows)
+            if (full0)
+              tma_store_3d(&p.tm_cache[t.seg], ch * nc + col0, 0, blk0, stg_w);
+            if (full1)
+              tma_store_3d(&p.tm_cache[t.seg], ch * nc + col0, 0, blk1,
+                           stg_w + 16 * 128);
+            bulk_commit();
+          }
+          if (any_rows) {
+            // the other coded rows: 8 lanes per 128-byte row, four rows
+            // per store instruction
+            for (int r0 = 0; r0 < 32; r0 += 4) {
+              const int r = r0 + (lane >> 3);
+              const int sub = lane & 7;
+              char* rp = reinterpret_cast<char*>(__shfl_sync(
+                  0xFFFFFFFFu, reinterpret_cast<uintptr_t>(rowp), r));
+              const uint4 val = *reinterpret_cast<const uint4*>(
+                  stg_w + r * 128 + ((sub ^ (r & 7)) << 4));
+              if (rp)
+                *reinterpret_cast<uint4*>(rp + (int64_t)(ch * nc + col0) * 2 +
+                                          sub * 16) = val;
+            }
           }
           __syncwarp();
         }
         KVTC_TR(3)
       }
     }
-    if constexpr (!kPaged) {
-      if (lane == 0) bulk_wait<0>();
-    }
+    if (lane == 0) bulk_wait<0>();
     KVTC_TR(0)
     KVTC_TR_SAVE(0)
     if (!ok && lane == 0) raise_abort(abort_flag, p.status);
@@ -1250,7 +1276,7 @@ __global__ void __launch_bounds__(256) paged_raw_kernel(
       atomicOr(p.status, KVTC_FLAG_BLOCK);
       continue;
     }
-    const uint4 v = ld_nc_v4(p.src[r] + (int64_t)j * p.sbytes[r] +
+    const uint4 v = ld_nc_v4(p.src[r] + (int64_t)p.sidx[j] * p.sbytes[r] +
                              (int64_t)rr * row_bytes + col * 16);
     char* dst = p.cache[j] +
                 ((int64_t)blk * p.block_size + tok % p.block_size) * row_bytes +
