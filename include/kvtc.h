@@ -258,6 +258,37 @@ int kvtc_fields_unpack(const kvtc_calib* calib, int layer0, int nlayers,
                        int64_t dst_bytes, void* cuda_stream);
 
 /*
+ * kvtc_decompress_packed -- the restore of kvtc_decompress (the mapping of
+ * technical summary 2A inverted: dequantise, project back with V_kept^T, add
+ * mu) read straight from the packed streams that kvtc_fields_pack wrote: the
+ * restore kernel unpacks each record's fields as it loads it, so the packed
+ * bytes are the only compressed bytes read and no codec stream is written.
+ * The output is bit-identical to kvtc_fields_unpack followed by
+ * kvtc_decompress.
+ *   src, src_bytes : the packed streams, in device memory or pinned host
+ *                    memory (read by the kernels over the host link, zero
+ *                    copy); pageable host memory is refused (EINVAL).
+ *   offsets        : int64 [n + 1] as kvtc_fields_pack wrote them (n =
+ *                    selected streams), device or pinned host memory.
+ *   T, dst, ld, cuda_stream, layer_events : as for kvtc_decompress.
+ * Each stream's header, slot table and length are checked against its
+ * calibration, T, the offsets and src_bytes on the GPU before anything they
+ * frame is read; a stream that does not match restores its coded tokens as
+ * from all-zero records and flags KVTC_FLAG_FORMAT; its raw rows are copied
+ * only when its magic, T_c and extent (both offsets on the 16-byte grid,
+ * inside src_bytes) check out.
+ * Kernel launches as for kvtc_decompress (the raw rows of a call with no
+ * coded token take one copy launch per 96 streams).  Streams must keep at
+ * most 15 groups, else ENOTSUP.  src 16-byte aligned, offsets 8.
+ * Errors: EINVAL, ESIZE, EALIGN, ENOTSUP, ENOMEM, ECUDA.
+ */
+int kvtc_decompress_packed(const kvtc_calib* calib, int layer0, int nlayers,
+                           int kv_mask, const void* src, int64_t src_bytes,
+                           const int64_t* offsets, int64_t T,
+                           void* const* dst, int64_t ld, void* cuda_stream,
+                           void* const* layer_events);
+
+/*
  * kvtc_calibrate -- the one-time calibration of technical summary 2A, on
  * the GPU, writing a version-1 blob (format above).  Per stream: mu = mean of
  * the calibration rows; V = eigenvectors of their covariance, sorted by

@@ -7,7 +7,8 @@ mirror the C ABI in ``include/kvtc.h``:
     kvtc_calib_load, kvtc_calib_free, kvtc_calib_query, kvtc_stream_bytes,
     kvtc_compress, kvtc_decompress, kvtc_decompress_paged,
     kvtc_fields_bound, kvtc_fields_workspace_bytes, kvtc_fields_pack,
-    kvtc_fields_unpack, kvtc_device_status, kvtc_launch_count, kvtc_strerror
+    kvtc_fields_unpack, kvtc_decompress_packed, kvtc_device_status,
+    kvtc_launch_count, kvtc_strerror
 
 Tensor arguments are torch CUDA tensors (or raw integer device addresses);
 ``stream`` defaults to torch's current stream.  There is no CPU fallback: if
@@ -91,6 +92,9 @@ def lib() -> ctypes.CDLL:
                                    c_vp, c_i64, c_vp, c_vp, c_i64, c_vp]),
         "kvtc_fields_unpack": (c_i, [c_vp, c_i, c_i, c_i, c_vp, c_i64, c_vp,
                                      c_i64, c_vp, c_i64, c_vp]),
+        "kvtc_decompress_packed": (c_i, [c_vp, c_i, c_i, c_i, c_vp, c_i64,
+                                         c_vp, c_i64, c_pp, c_i64, c_vp,
+                                         c_pp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -235,16 +239,36 @@ def kvtc_decompress(calib: Calib, layer0: int, nlayers: int, kv_mask: int,
                     src, src_bytes: int, T: int, dst: Sequence, ld: int,
                     stream=None, layer_events: Optional[Sequence] = None
                     ) -> None:
-    ev = None
-    if layer_events is not None:
-        ev = (ctypes.c_void_p * max(1, len(layer_events)))()
-        for i, e in enumerate(layer_events):
-            ev[i] = e if isinstance(e, int) else int(e.cuda_event)
     _check(lib().kvtc_decompress(calib.handle, layer0, nlayers, kv_mask,
                                  _ptr(src) or None, src_bytes, T,
                                  _ptr_array(dst), ld,
-                                 _stream(stream) or None, ev),
+                                 _stream(stream) or None,
+                                 _event_array(layer_events)),
            "kvtc_decompress")
+
+
+def _event_array(layer_events):
+    if layer_events is None:
+        return None
+    ev = (ctypes.c_void_p * max(1, len(layer_events)))()
+    for i, e in enumerate(layer_events):
+        ev[i] = e if isinstance(e, int) else int(e.cuda_event)
+    return ev
+
+
+def kvtc_decompress_packed(calib: Calib, layer0: int, nlayers: int,
+                           kv_mask: int, src, src_bytes: int, offsets,
+                           T: int, dst: Sequence, ld: int, stream=None,
+                           layer_events: Optional[Sequence] = None) -> None:
+    """Restore from packed streams (offsets as kvtc_fields_pack wrote);
+    src and offsets device or pinned host tensors."""
+    _check(lib().kvtc_decompress_packed(calib.handle, layer0, nlayers,
+                                        kv_mask, _ptr(src) or None, src_bytes,
+                                        _ptr(offsets) or None, T,
+                                        _ptr_array(dst), ld,
+                                        _stream(stream) or None,
+                                        _event_array(layer_events)),
+           "kvtc_decompress_packed")
 
 
 def kvtc_decompress_paged(calib: Calib, layer0: int, nlayers: int,

@@ -44,7 +44,6 @@ static_assert(kNarrowK / 16 <= 15, "at most 30 field slots (one warp)");
 constexpr int kFpThreads = 256;
 constexpr int kFpWarps = kFpThreads / 32;
 constexpr int kFpLayoutThreads = 1024;
-constexpr uint32_t kFpMagic = 0x5046564Bu;  // "KVFP", little-endian
 constexpr int kFpBuf = kFpRawChunk;              // one input buffer
 constexpr int kFpSmem = 3 * kFpBuf + 256 + 16;   // 2 in, 1 out + padding
 

@@ -293,7 +293,24 @@ bool raw_list_add(RawList& r, const char* s, char* d, int64_t sld,
   g.rows = (int32_t)rows;
   g.row_bytes = (int32_t)row_bytes;
   g.chunk_begin = r.total_chunks;
+  g.pk = -1;
+  g.pk_tc = 0;
+  g.pk_off = 0;
   r.total_chunks += rows * (row_bytes / 16);
+  return true;
+}
+
+// The same for rows of packed stream `pk` (r.pk_offs), `at` bytes from its
+// start, whose header must hold T_c = tc; the kernel checks both.
+bool raw_list_add_packed(RawList& r, int pk, int tc, int64_t at, char* d,
+                         int64_t dld, int64_t rows, int64_t row_bytes) {
+  if (!raw_list_add(r, nullptr, d, row_bytes, dld, rows, row_bytes))
+    return false;
+  if (rows <= 0 || row_bytes <= 0) return true;
+  RawListSeg& g = r.seg[r.nseg - 1];
+  g.pk = pk;
+  g.pk_tc = tc;
+  g.pk_off = at;
   return true;
 }
 
@@ -320,6 +337,192 @@ int resolve_input(const void* p, const void** dev) {
     return KVTC_OK;
   }
   return KVTC_EINVAL;
+}
+
+// Restore of codec streams (pk_offs null), or of the packed streams that
+// kvtc_fields_pack wrote (pk_offs: their offsets), whose records the restore
+// kernel unpacks as it reads them.
+int decompress_impl(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
+                    const void* src, int64_t src_bytes,
+                    const int64_t* pk_offs, int64_t T, void* const* dst,
+                    int64_t ld, void* cuda_stream,
+                    void* const* layer_events) {
+  const bool packed = pk_offs != nullptr;
+  if (!c || !dst || (!src && src_bytes) || T < 0 || T > (1LL << 31) - 1)
+    return KVTC_EINVAL;
+  std::vector<int> cs, slot;
+  int st = select_streams(c, layer0, nlayers, kv_mask, &cs, &slot);
+  if (st != KVTC_OK) return st;
+  int64_t s_, w_, tc;
+  split_tokens(T, c->sink, c->window, &s_, &w_, &tc);
+  int64_t need = 0;
+  std::vector<int64_t> off(cs.size());
+  for (size_t i = 0; i < cs.size(); ++i) {
+    const HostStream& h = c->hs[cs[i]];
+    if (!dst[slot[i]] && T > 0) return KVTC_EINVAL;
+    if (ld < h.D) return KVTC_ESIZE;
+    if (ld % 8 || !aligned16(dst[slot[i]])) return KVTC_EALIGN;
+    // field packing holds at most 15 active groups a stream
+    if (packed && h.Ga > 15) return KVTC_ENOTSUP;
+    off[i] = need;
+    need += stream_bytes_of(c, h, T);
+  }
+  // a packed stream is at least 256 bytes; its length is in the offsets,
+  // which the kernels check against src_bytes
+  if (packed) need = (int64_t)cs.size() * 256;
+  if (src_bytes < need) return KVTC_ESIZE;
+  if (!aligned16(src)) return KVTC_EALIGN;
+  if (packed && (reinterpret_cast<uintptr_t>(pk_offs) & 7u))
+    return KVTC_EALIGN;
+  if (layer_events)
+    for (int l = 0; l < nlayers; ++l)
+      if (!layer_events[l]) return KVTC_EINVAL;
+  DeviceGuard guard(c->device);
+  if (!guard.ok) return KVTC_ECUDA;
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  if (need > 0) {
+    st = resolve_input(src, &src);
+    if (st != KVTC_OK) return st;
+  }
+  if (packed && !cs.empty()) {
+    const void* o = pk_offs;
+    st = resolve_input(pk_offs, &o);
+    if (st != KVTC_OK) return st;
+    pk_offs = static_cast<const int64_t*>(o);
+  }
+  const char* in = static_cast<const char*>(src);
+
+  // Launch groups: all streams at once, or one layer at a time when the
+  // caller wants per-layer completion events.
+  std::vector<std::pair<size_t, size_t>> groups;
+  if (layer_events) {
+    size_t i = 0;
+    for (int l = 0; l < nlayers; ++l) {
+      size_t j = i;
+      while (j < cs.size() && slot[j] / 2 == l) ++j;
+      groups.push_back({i, j});
+      i = j;
+    }
+  } else {
+    for (size_t i = 0; i < cs.size(); i += kDecMaxSeg)
+      groups.push_back({i, std::min(cs.size(), i + (size_t)kDecMaxSeg)});
+  }
+  RawParams* rp = new (std::nothrow) RawParams;
+  DecParams* p = new (std::nothrow) DecParams;
+  if (!rp || !p) {
+    delete rp;
+    delete p;
+    return KVTC_ENOMEM;
+  }
+  int ret = KVTC_OK;
+  for (size_t gi = 0; gi < groups.size() && ret == KVTC_OK; ++gi) {
+    const size_t i0 = groups[gi].first, i1 = groups[gi].second;
+    // raw rows back to their places: by the decompress kernel while it
+    // runs, or by a copy kernel when there are no coded tokens
+    std::memset(rp, 0, sizeof(*rp));
+    std::memset(p, 0, sizeof(*p));
+    if (packed) {
+      p->raw.pk_base = reinterpret_cast<const uint8_t*>(in);
+      p->raw.pk_offs = pk_offs;
+      p->raw.pk_bytes = src_bytes;
+    }
+    for (size_t i = i0; i < i1; ++i) {
+      const HostStream& h = c->hs[cs[i]];
+      const int64_t rb = 2LL * h.D;
+      const char* so = in + off[i];
+      char* x = static_cast<char*>(dst[slot[i]]);
+      const int64_t rows[2] = {s_, w_};
+      const char* s2[2] = {so, so + s_ * rb};
+      char* d2[2] = {x, x + (T - w_) * 2 * ld};
+      for (int k2 = 0; k2 < 2; ++k2) {
+        if (rows[k2] <= 0) continue;
+        if (packed) {
+          // the rows follow the header and the slot table (4 G_a bytes,
+          // padded to 16)
+          const int64_t at =
+              kFpHeader + ((4 * h.Ga + 15) & ~15) + (k2 ? s_ * rb : 0);
+          if (!raw_list_add_packed(p->raw, (int)i, (int)tc, at, d2[k2],
+                                   2 * ld, rows[k2], rb))
+            ret = KVTC_EINVAL;
+          continue;
+        }
+        if (tc > 0) {
+          if (!raw_list_add(p->raw, s2[k2], d2[k2], rb, 2 * ld, rows[k2], rb))
+            ret = KVTC_EINVAL;
+          continue;
+        }
+        if (rp->nseg == kRawMaxSeg) {
+          if (launch_raw_copy(*rp, stream) != cudaSuccess) ret = KVTC_ECUDA;
+          rp->nseg = 0;
+          rp->total_chunks = 0;
+        }
+        RawSeg& g = rp->seg[rp->nseg++];
+        g.src = s2[k2];
+        g.dst = d2[k2];
+        g.src_ld = rb;
+        g.dst_ld = 2 * ld;
+        g.rows = (int32_t)rows[k2];
+        g.row_bytes = (int32_t)rb;
+        g.chunk_begin = rp->total_chunks;
+        rp->total_chunks += rows[k2] * (rb / 16);
+      }
+    }
+    if (rp->nseg && launch_raw_copy(*rp, stream) != cudaSuccess)
+      ret = KVTC_ECUDA;
+    if (packed && tc == 0 &&
+        launch_raw_list(p->raw, c->d_status, stream) != cudaSuccess)
+      ret = KVTC_ECUDA;
+    if (ret != KVTC_OK) break;
+    if (tc > 0) {
+      int tiles = 0;
+      for (size_t i = i0; i < i1; ++i) {
+        const HostStream& h = c->hs[cs[i]];
+        DecSeg& g = p->seg[i - i0];
+        // packed input: the kernel finds the records through the offsets
+        g.rec = reinterpret_cast<const uint8_t*>(
+            packed ? in : in + off[i] + (s_ + w_) * 2LL * h.D);
+        g.dst = static_cast<char*>(dst[slot[i]]) + s_ * 2 * ld;
+        g.ld_bytes = 2 * ld;
+        g.tc = (int32_t)tc;
+        g.cs = cs[i];
+        if (!encode_store_2d(&p->tm_out[i - i0], g.dst, (uint64_t)h.D,
+                             (uint64_t)tc, 2ull * ld)) {
+          ret = KVTC_ECUDA;
+          break;
+        }
+        tiles += (int)((tc + kPairM - 1) / kPairM);
+      }
+      if (ret != KVTC_OK) break;
+      p->streams = c->d_streams;
+      p->status = c->d_status;
+      p->nseg = (int32_t)(i1 - i0);
+      p->total_tiles = tiles;
+      p->tiles_per_seg = (int32_t)((tc + kPairM - 1) / kPairM);
+      int rmax = 0, kmax = 0;
+      for (size_t i = i0; i < i1; ++i) {
+        rmax = std::max(rmax, c->hs[cs[i]].R);
+        kmax = std::max(kmax, c->hs[cs[i]].k);
+      }
+      p->rec_words = rmax / 4;
+      p->wide = kmax > kNarrowK;
+      p->packed = packed;
+      p->pk_first = (int32_t)i0;
+      p->pk_raw_rows = (int32_t)(s_ + w_);
+      p->nstages = decompress_stages(p->rec_words);
+      const int mp = max_pairs_decompress(
+          decompress_smem_bytes(p->nstages, p->rec_words));
+      if (tiles && (mp < 1 || launch_decompress(*p, pairs_for(mp, tiles),
+                                                stream) != cudaSuccess))
+        ret = KVTC_ECUDA;
+    }
+    if (ret == KVTC_OK && layer_events &&
+        cudaEventRecord(static_cast<cudaEvent_t>(layer_events[gi]), stream) !=
+            cudaSuccess)
+      ret = KVTC_ECUDA;
+  }
+  delete rp;
+  delete p;
+  return ret;
 }
 
 }  // namespace
@@ -758,146 +961,18 @@ int kvtc_decompress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
                     const void* src, int64_t src_bytes, int64_t T,
                     void* const* dst, int64_t ld, void* cuda_stream,
                     void* const* layer_events) {
-  if (!c || !dst || (!src && src_bytes) || T < 0 || T > (1LL << 31) - 1)
-    return KVTC_EINVAL;
-  std::vector<int> cs, slot;
-  int st = select_streams(c, layer0, nlayers, kv_mask, &cs, &slot);
-  if (st != KVTC_OK) return st;
-  int64_t s_, w_, tc;
-  split_tokens(T, c->sink, c->window, &s_, &w_, &tc);
-  int64_t need = 0;
-  std::vector<int64_t> off(cs.size());
-  for (size_t i = 0; i < cs.size(); ++i) {
-    const HostStream& h = c->hs[cs[i]];
-    if (!dst[slot[i]] && T > 0) return KVTC_EINVAL;
-    if (ld < h.D) return KVTC_ESIZE;
-    if (ld % 8 || !aligned16(dst[slot[i]])) return KVTC_EALIGN;
-    off[i] = need;
-    need += stream_bytes_of(c, h, T);
-  }
-  if (src_bytes < need) return KVTC_ESIZE;
-  if (!aligned16(src)) return KVTC_EALIGN;
-  if (layer_events)
-    for (int l = 0; l < nlayers; ++l)
-      if (!layer_events[l]) return KVTC_EINVAL;
-  DeviceGuard guard(c->device);
-  if (!guard.ok) return KVTC_ECUDA;
-  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-  if (need > 0) {
-    st = resolve_input(src, &src);
-    if (st != KVTC_OK) return st;
-  }
-  const char* in = static_cast<const char*>(src);
+  return decompress_impl(c, layer0, nlayers, kv_mask, src, src_bytes, nullptr,
+                         T, dst, ld, cuda_stream, layer_events);
+}
 
-  // Launch groups: all streams at once, or one layer at a time when the
-  // caller wants per-layer completion events.
-  std::vector<std::pair<size_t, size_t>> groups;
-  if (layer_events) {
-    size_t i = 0;
-    for (int l = 0; l < nlayers; ++l) {
-      size_t j = i;
-      while (j < cs.size() && slot[j] / 2 == l) ++j;
-      groups.push_back({i, j});
-      i = j;
-    }
-  } else {
-    for (size_t i = 0; i < cs.size(); i += kDecMaxSeg)
-      groups.push_back({i, std::min(cs.size(), i + (size_t)kDecMaxSeg)});
-  }
-  RawParams* rp = new (std::nothrow) RawParams;
-  DecParams* p = new (std::nothrow) DecParams;
-  if (!rp || !p) {
-    delete rp;
-    delete p;
-    return KVTC_ENOMEM;
-  }
-  int ret = KVTC_OK;
-  for (size_t gi = 0; gi < groups.size() && ret == KVTC_OK; ++gi) {
-    const size_t i0 = groups[gi].first, i1 = groups[gi].second;
-    // raw rows back to their places: by the decompress kernel while it
-    // runs, or by a copy kernel when there are no coded tokens
-    std::memset(rp, 0, sizeof(*rp));
-    std::memset(p, 0, sizeof(*p));
-    for (size_t i = i0; i < i1; ++i) {
-      const HostStream& h = c->hs[cs[i]];
-      const int64_t rb = 2LL * h.D;
-      const char* so = in + off[i];
-      char* x = static_cast<char*>(dst[slot[i]]);
-      const int64_t rows[2] = {s_, w_};
-      const char* s2[2] = {so, so + s_ * rb};
-      char* d2[2] = {x, x + (T - w_) * 2 * ld};
-      for (int k2 = 0; k2 < 2; ++k2) {
-        if (rows[k2] <= 0) continue;
-        if (tc > 0) {
-          if (!raw_list_add(p->raw, s2[k2], d2[k2], rb, 2 * ld, rows[k2], rb))
-            ret = KVTC_EINVAL;
-          continue;
-        }
-        if (rp->nseg == kRawMaxSeg) {
-          if (launch_raw_copy(*rp, stream) != cudaSuccess) ret = KVTC_ECUDA;
-          rp->nseg = 0;
-          rp->total_chunks = 0;
-        }
-        RawSeg& g = rp->seg[rp->nseg++];
-        g.src = s2[k2];
-        g.dst = d2[k2];
-        g.src_ld = rb;
-        g.dst_ld = 2 * ld;
-        g.rows = (int32_t)rows[k2];
-        g.row_bytes = (int32_t)rb;
-        g.chunk_begin = rp->total_chunks;
-        rp->total_chunks += rows[k2] * (rb / 16);
-      }
-    }
-    if (rp->nseg && launch_raw_copy(*rp, stream) != cudaSuccess)
-      ret = KVTC_ECUDA;
-    if (ret != KVTC_OK) break;
-    if (tc > 0) {
-      int tiles = 0;
-      for (size_t i = i0; i < i1; ++i) {
-        const HostStream& h = c->hs[cs[i]];
-        DecSeg& g = p->seg[i - i0];
-        g.rec = reinterpret_cast<const uint8_t*>(in + off[i] +
-                                                 (s_ + w_) * 2LL * h.D);
-        g.dst = static_cast<char*>(dst[slot[i]]) + s_ * 2 * ld;
-        g.ld_bytes = 2 * ld;
-        g.tc = (int32_t)tc;
-        g.cs = cs[i];
-        if (!encode_store_2d(&p->tm_out[i - i0], g.dst, (uint64_t)h.D,
-                             (uint64_t)tc, 2ull * ld)) {
-          ret = KVTC_ECUDA;
-          break;
-        }
-        tiles += (int)((tc + kPairM - 1) / kPairM);
-      }
-      if (ret != KVTC_OK) break;
-      p->streams = c->d_streams;
-      p->status = c->d_status;
-      p->nseg = (int32_t)(i1 - i0);
-      p->total_tiles = tiles;
-      p->tiles_per_seg = (int32_t)((tc + kPairM - 1) / kPairM);
-      int rmax = 0, kmax = 0;
-      for (size_t i = i0; i < i1; ++i) {
-        rmax = std::max(rmax, c->hs[cs[i]].R);
-        kmax = std::max(kmax, c->hs[cs[i]].k);
-      }
-      p->rec_words = rmax / 4;
-      p->wide = kmax > kNarrowK;
-      p->nstages = decompress_stages(p->rec_words);
-      const int mp = max_pairs_decompress(
-          decompress_smem_bytes(p->nstages, p->rec_words));
-      if (tiles && (mp < 1 || launch_decompress(*p, pairs_for(mp, tiles),
-                                                stream) != cudaSuccess))
-        ret = KVTC_ECUDA;
-    }
-    if (ret == KVTC_OK && layer_events &&
-        cudaEventRecord(static_cast<cudaEvent_t>(layer_events[gi]), stream) !=
-            cudaSuccess)
-      ret = KVTC_ECUDA;
-  }
-  delete rp;
-  delete p;
-  return ret;
+int kvtc_decompress_packed(const kvtc_calib* c, int layer0, int nlayers,
+                           int kv_mask, const void* src, int64_t src_bytes,
+                           const int64_t* offsets, int64_t T, void* const* dst,
+                           int64_t ld, void* cuda_stream,
+                           void* const* layer_events) {
+  if (!offsets) return KVTC_EINVAL;
+  return decompress_impl(c, layer0, nlayers, kv_mask, src, src_bytes, offsets,
+                         T, dst, ld, cuda_stream, layer_events);
 }
 
 int kvtc_decompress_paged(const kvtc_calib* c, int layer0, int nlayers,

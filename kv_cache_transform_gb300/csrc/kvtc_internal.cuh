@@ -50,12 +50,21 @@ struct RawListSeg {
   int32_t rows;             // rows to copy
   int32_t row_bytes;        // bytes per row (multiple of 16)
   int64_t chunk_begin;      // first 16-byte chunk index of this segment
+  int32_t pk;               // >= 0: the rows sit in packed stream pk, at
+                            // pk_off bytes from its start (src unused)
+  int32_t pk_tc;            // the T_c its header must hold
+  int64_t pk_off;
 };
 struct RawList {
   RawListSeg seg[kRawListMax];
   int32_t nseg;
   int32_t pad;
   int64_t total_chunks;
+  // packed input (kvtc_decompress_packed): stream i spans
+  // [pk_offs[i], pk_offs[i + 1]) of pk_base, pk_bytes in all
+  const uint8_t* pk_base;
+  const int64_t* pk_offs;
+  int64_t pk_bytes;
 };
 
 // ---------------------------------------------------------------- compress
@@ -107,8 +116,11 @@ struct DecParams {
   int32_t nstages;          // B ring depth (shared-memory stages)
   int32_t rec_words;        // record staging words per thread (max R / 4)
   int32_t wide;             // a stream has k + 16 > 256: one A buffer
-  int32_t pad2;
-  RawList raw;              // sink/window rows of these streams
+  int32_t packed;           // records come from packed streams (below)
+  int32_t pk_first;         // packed stream index of segment 0
+  int32_t pk_raw_rows;      // s' + w' (every stream of a call has one T)
+  RawList raw;              // sink/window rows of these streams; for packed
+                            // input also pk_base, pk_offs and pk_bytes
 };
 // every stream's sink, window and padding segments fit one launch's list
 static_assert(3 * kCompMaxSeg <= kRawListMax, "raw list too short");
@@ -183,6 +195,7 @@ constexpr int kFpWorkWords = 32;      // u32 words per (stream, chunk)
 constexpr int kFpRawChunk = 32768;    // raw-row bytes per copy item; a
                                       // record tile is at most this long
 constexpr int kFpHeader = 16;         // packed stream header bytes
+constexpr uint32_t kFpMagic = 0x5046564Bu;  // "KVFP", little-endian
 struct FpStream {
   int64_t in_off;       // pack: codec stream offset in the input
   int64_t out_off;      // unpack: codec stream offset in the output
@@ -223,6 +236,9 @@ cudaError_t launch_raw_copy(const RawParams& p, cudaStream_t st);
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns,
                                  cudaStream_t st);
 cudaError_t launch_paged_raw(const PagedParams& p, cudaStream_t st);
+// Raw rows of packed streams with no coded token (a RawList on its own).
+cudaError_t launch_raw_list(const RawList& r, unsigned* status,
+                            cudaStream_t st);
 // Field packing (kvtc_fieldpack.cu): the three pack launches, and unpack.
 cudaError_t launch_fields_pack(const FpParams& p, cudaStream_t st);
 cudaError_t launch_fields_unpack(const FpParams& p, cudaStream_t st);

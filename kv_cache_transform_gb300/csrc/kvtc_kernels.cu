@@ -20,6 +20,7 @@
 //
 // Every mbarrier wait is bounded; a wait that runs out sets a sticky flag
 // and the CTA drains its own copies and MMAs, frees TMEM and returns.
+#include <algorithm>
 #include <type_traits>
 
 #include "../../include/kvtc.h"
@@ -169,9 +170,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 // Raw rows (sink and window, and zero padding) of a RawList, copied in
 // 16-byte chunks by the `stride` threads of the raw-copy role across the
 // grid (thread `tid` of them), four chunks in flight per thread.  Runs
-// beside the tensor-core work of the same kernel.
+// beside the tensor-core work of the same kernel.  kPk: segments may sit in
+// packed streams (restore from packed input).
+template <bool kPk = false>
 __device__ __forceinline__ void raw_list_copy(const RawList& r, int64_t tid,
-                                              int64_t stride) {
+                                              int64_t stride,
+                                              unsigned* status) {
   int sg = 0;  // chunks visit increasing indices, so the segment only grows
   for (int64_t c0 = tid; c0 < r.total_chunks; c0 += 4 * stride) {
     uint4 v[4];
@@ -188,7 +192,26 @@ __device__ __forceinline__ void raw_list_copy(const RawList& r, int64_t tid,
         const int64_t local = c - g.chunk_begin;
         const int64_t row = local / cpr;
         const int64_t col = local - row * cpr;
-        if (g.src) v[u] = ld_nc_v4(g.src + row * g.src_ld + col * 16);
+        const char* src = g.src;
+        if (kPk && g.pk >= 0) {
+          // rows of a packed stream: found through its offsets, and only
+          // read when they lie inside the stream and the input
+          const int64_t o0 = r.pk_offs[g.pk], o1 = r.pk_offs[g.pk + 1];
+          const int64_t need = g.pk_off + (int64_t)g.rows * g.row_bytes;
+          src = nullptr;
+          if (o0 >= 0 && ((o0 | o1) & 15) == 0 && o1 >= o0 + need &&
+              o1 <= r.pk_bytes) {
+            const uint32_t* hd =
+                reinterpret_cast<const uint32_t*>(r.pk_base + o0);
+            if (__ldg(hd) == kFpMagic && (int32_t)__ldg(hd + 1) == g.pk_tc)
+              src = reinterpret_cast<const char*>(r.pk_base) + o0 + g.pk_off;
+          }
+          if (!src) {
+            if (col == 0 && row == 0) atomicOr(status, KVTC_FLAG_FORMAT);
+            continue;
+          }
+        }
+        if (src) v[u] = ld_nc_v4(src + row * g.src_ld + col * 16);
         d[u] = g.dst + row * g.dst_ld + col * 16;
       }
     }
@@ -196,6 +219,14 @@ __device__ __forceinline__ void raw_list_copy(const RawList& r, int64_t tid,
     for (int u = 0; u < 4; ++u)
       if (d[u]) *reinterpret_cast<uint4*>(d[u]) = v[u];
   }
+}
+
+// Raw rows of packed streams that have no coded token: the RawList copy on
+// its own, every thread of the grid one copier.
+__global__ void __launch_bounds__(256)
+    raw_list_kernel(const __grid_constant__ RawList r, unsigned* status) {
+  raw_list_copy<true>(r, (int64_t)blockIdx.x * 256 + threadIdx.x,
+                      (int64_t)gridDim.x * 256, status);
 }
 
 // ======================================================================
@@ -283,13 +314,18 @@ __device__ __forceinline__ DecTile resolve(const PagedParams& p, int item) {
   return t;
 }
 
-// kWide: a launch holding a stream with k > 240 (one 256-column A buffer,
-// and B stages of up to two per chunk); otherwise the double-buffered
-// layout with one B stage per chunk.  A template parameter, so that the
-// narrow kernels carry none of the wide layout's state.
-template <class P, bool kWide>
+// kLayout of a launch: 0 (narrow) when every stream has k <= 240: two
+// 128-column A buffers, one B stage per chunk; 2 (wide) when a stream has
+// k > 240: one 256-column A buffer and up to two B stages per chunk; 3 the
+// narrow layout reading its records from packed streams (field packing
+// holds at most 15 groups).  A template parameter, so that the narrow
+// kernel carries none of the others' state.
+template <class P, int kLayout>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
     decompress_kernel(const __grid_constant__ P p) {
+  constexpr bool kWide = kLayout == 2;
+  // kLayout 3: narrow, records read from packed streams
+  constexpr bool kPacked = kLayout == 3;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int nst = p.nstages;
@@ -538,6 +574,101 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       const int lo = max(-rec0, 0);
       const int hi = min(max(t.tc - rec0, 0), 32);
       const uint8_t* rbase = t.rec + (int64_t)rec0 * R;
+      // Packed input: the stream's header and slot table (lane s = field
+      // slot s: vmin, code bits d, bit position of its code), checked
+      // against the calibration, T and the offsets before anything they
+      // frame is read; its records are Rp bytes long.
+      int pk_vmin = 0, pk_d = 0, pk_pos = 0, pk_hb2 = 0, pk_rp = 0;
+      bool pk_ok = false;
+      if constexpr (kPacked) {
+        const int si = t.seg + p.pk_first, ns = 2 * Ga;
+        const int64_t o0 = p.raw.pk_offs[si], o1 = p.raw.pk_offs[si + 1];
+        const int tb = (4 * Ga + 15) & ~15;
+        const int64_t rawb = (int64_t)p.pk_raw_rows * ds->D * 2;
+        const bool in = o0 >= 0 && (o0 & 15) == 0 && (o1 & 15) == 0 &&
+                        o1 >= o0 + kFpHeader + tb && o1 <= p.raw.pk_bytes;
+        const uint8_t* sb = p.raw.pk_base + (in ? o0 : 0);
+        uint32_t hw = 0, te = 0;
+        if (in && lane < 4)
+          hw = __ldg(reinterpret_cast<const uint32_t*>(sb) + lane);
+        if (in && lane < ns)
+          te = __ldg(reinterpret_cast<const uint16_t*>(sb + kFpHeader) + lane);
+        pk_vmin = (int)(te & 0xFFu);
+        pk_d = (int)(te >> 8);
+        const int wbits = lane < ns ? pk_d + 2 : 0;
+        int incl = wbits;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        pk_pos = incl - wbits;
+        pk_hb2 = (__shfl_sync(0xFFFFFFFFu, incl, 31) + 15) >> 4;
+        const int used = __shfl_sync(0xFFFFFFFFu, my_po, Ga - 1) +
+                         2 * __shfl_sync(0xFFFFFFFFu, my_b, Ga - 1);
+        pk_rp = used - 2 * Ga + 2 * pk_hb2;
+        const uint32_t h0 = __shfl_sync(0xFFFFFFFFu, hw, 0);
+        const uint32_t h1 = __shfl_sync(0xFFFFFFFFu, hw, 1);
+        const uint32_t h2 = __shfl_sync(0xFFFFFFFFu, hw, 2);
+        const bool slot_ok = lane >= ns || (pk_d <= 6 && pk_vmin <= 63);
+        pk_ok = __all_sync(0xFFFFFFFFu, slot_ok) && in && h0 == kFpMagic &&
+                (int)h1 == t.tc && (int)(h2 & 0xFFFFu) == pk_rp &&
+                (int)(h2 >> 16) == ns &&
+                o0 + kFpHeader + tb + rawb + (int64_t)t.tc * pk_rp <= o1;
+        if (!pk_ok) {
+          // decoded as all-zero records: zero fields, codes and planes
+          pk_vmin = pk_d = pk_pos = pk_hb2 = 0;
+          if (lane == 0 && q == 0 && rank == 0)
+            atomicOr(p.status, KVTC_FLAG_FORMAT);
+        }
+        rbase = sb + kFpHeader + tb + rawb + (int64_t)row0 * pk_rp;
+      }
+      if constexpr (kPacked) {
+        // the warp's packed records are 32 Rp contiguous bytes (16-byte
+        // aligned: Rp is even and the stream's regions are multiples of
+        // 16); coalesced 16-byte loads, each halfword stored at its token's
+        // place in the word-transposed staging
+        const int nvalid = pk_ok ? min(max(t.tc - row0, 0), 32) : 0;
+        // tokens without a record (past T_c, or all of an invalid stream)
+        // decode from zeros, as in the codec layout
+        if (nvalid < 32) {
+          const int nz = 32 - nvalid;
+          for (int i = lane; i < rec_words * nz; i += 32)
+            stg[(i / nz) * 33 + nvalid + i % nz] = 0u;
+        }
+        const int hpr = pk_rp >> 1;
+        const int nchunk = (nvalid * pk_rp + 15) >> 4;
+        const uint32_t stg_a = smem_u32(stg);
+        for (int c0 = 0; c0 < nchunk; c0 += 8 * 32) {
+          uint4 v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int c = c0 + u * 32 + lane;
+            v[u] = c < nchunk ? ld_nc_v4(rbase + 16 * c)
+                              : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int c = c0 + u * 32 + lane;
+            if (c < nchunk) {
+              const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+              int tr = (8 * c) / hpr;
+              int idx = 8 * c - tr * hpr;
+#pragma unroll
+              for (int h = 0; h < 8; ++h) {
+                if (tr < nvalid)
+                  sts_u16(stg_a + (uint32_t)((((idx >> 1) * 33 + tr) << 2) +
+                                             ((idx & 1) << 1)),
+                          (wv[h >> 1] >> ((h & 1) << 4)) & 0xFFFFu);
+                if (++idx == hpr) {
+                  idx = 0;
+                  ++tr;
+                }
+              }
+            }
+          }
+        }
+      } else {
       // Coalesced 16-byte loads of the warp's 32 records (up to eight in
       // flight per lane), stored word-transposed ([word][token], row pitch
       // 33) in shared memory; done before waiting for the A buffer so the
@@ -564,6 +695,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
           stg[(wd + 3) * 33 + tr] = v[u].w;
         }
       }
+      }
       KVTC_TR(2)
       if (!mbar_wait(&a_empty[abuf], (ause & 1u) ^ 1u, abort_flag)) {
         ok = false;
@@ -577,8 +709,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
           tmem + ((uint32_t)(q * 32) << 16) + 256u + abuf * 128u;
       for (int a = 0; a < Ga; ++a) {
         const int b = __shfl_sync(0xFFFFFFFFu, my_b, a);
-        const int po = __shfl_sync(0xFFFFFFFFu, my_po, a);
-        const uint32_t f = stg[a * 33 + lane];
+        int po = __shfl_sync(0xFFFFFFFFu, my_po, a);
+        uint32_t f;
+        if constexpr (kPacked) {
+          // packed record: the low bytes of the 2 Ga fields, the codes of
+          // their high bytes (per slot, v - vmin in d bits, then the high
+          // byte's low two bits), the bit-planes
+          const auto hword = [&](int i) -> uint32_t {
+            return i < rec_words * 2
+                       ? (stg[(i >> 1) * 33 + lane] >> ((i & 1) << 4)) & 0xFFFFu
+                       : 0u;
+          };
+          const auto high = [&](int sl) -> uint32_t {
+            const int vmin = __shfl_sync(0xFFFFFFFFu, pk_vmin, sl);
+            const int d = __shfl_sync(0xFFFFFFFFu, pk_d, sl);
+            const int pos = __shfl_sync(0xFFFFFFFFu, pk_pos, sl);
+            const int i = Ga + (pos >> 4);
+            const uint32_t bits = hword(i) | (hword(i + 1) << 16);
+            const uint32_t code = (bits >> (pos & 15)) & ((4u << d) - 1u);
+            return ((((code & ((1u << d) - 1u)) + (uint32_t)vmin) << 2) |
+                    (code >> d)) & 0xFFu;
+          };
+          const uint32_t lo16 = hword(a);
+          f = (lo16 & 0xFFu) | (high(2 * a) << 8) | ((lo16 >> 8) << 16) |
+              (high(2 * a + 1) << 24);
+          po = po - 2 * Ga + 2 * pk_hb2;  // planes follow the codes
+        } else {
+          f = stg[a * 33 + lane];
+        }
         uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
         switch (b) {  // uniform over the warp
           case 1: unpack_planes<1>(stg, po, lane, w0, w1, w2, w3); break;
@@ -623,8 +781,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
   } else if (warp >= 26) {
     // ------------------------------- raw rows (sink and window) back
     if constexpr (std::is_same<P, DecParams>::value)
-      raw_list_copy(p.raw, (int64_t)blockIdx.x * 64 + (warp - 26) * 32 + lane,
-                    (int64_t)gridDim.x * 64);
+      raw_list_copy<kPacked>(
+          p.raw, (int64_t)blockIdx.x * 64 + (warp - 26) * 32 + lane,
+          (int64_t)gridDim.x * 64, p.status);
   } else {
     // -------------- epilogue: bf16 rows (the mean came in the MMA)
     // Sixteen warps.  With 256 / nc accumulators, 16 nc / 256 warps read
@@ -1007,7 +1166,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
   } else if (warp >= 18) {
     // ---------------------------- raw rows (sink, window) and padding
     raw_list_copy(p.raw, (int64_t)blockIdx.x * 64 + (warp - 18) * 32 + lane,
-                  (int64_t)gridDim.x * 64);
+                  (int64_t)gridDim.x * 64, p.status);
   } else {
     // ------------------------- epilogue: quantise + bit-plane records
     // Four sets of four warps (one per TMEM lane quadrant each) share every
@@ -1334,9 +1493,9 @@ int max_pairs_compress(int smem_bytes) {
 }
 
 int max_pairs_decompress(int smem_bytes) {
-  allow_smem((const void*)decompress_kernel<DecParams, false>, 232448);
-  return max_pairs((const void*)decompress_kernel<DecParams, false>,
-                   kDecThreads, smem_bytes);
+  allow_smem((const void*)decompress_kernel<DecParams, 0>, 232448);
+  return max_pairs((const void*)decompress_kernel<DecParams, 0>, kDecThreads,
+                   smem_bytes);
 }
 
 cudaError_t launch_compress(const CompParams& p, int pairs, cudaStream_t st) {
@@ -1347,29 +1506,36 @@ cudaError_t launch_compress(const CompParams& p, int pairs, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <class P, bool kWide>
+template <class P, int kLayout>
 static cudaError_t launch_dec_as(const P& p, int pairs, cudaStream_t st) {
-  allow_smem((const void*)decompress_kernel<P, kWide>, 232448);
-  decompress_kernel<P, kWide>
+  allow_smem((const void*)decompress_kernel<P, kLayout>, 232448);
+  decompress_kernel<P, kLayout>
       <<<2 * pairs, kDecThreads, decompress_smem_bytes(p.nstages, p.rec_words),
          st>>>(p);
   count_launch();
   return cudaGetLastError();
 }
 
-template <class P>
-static cudaError_t launch_dec(const P& p, int pairs, cudaStream_t st) {
-  return p.wide ? launch_dec_as<P, true>(p, pairs, st)
-                : launch_dec_as<P, false>(p, pairs, st);
+cudaError_t launch_raw_list(const RawList& r, unsigned* status,
+                            cudaStream_t st) {
+  if (r.total_chunks <= 0) return cudaSuccess;
+  const int64_t b = (r.total_chunks + 1023) / 1024;
+  raw_list_kernel<<<(int)std::min<int64_t>(b, 4 * 152), 256, 0, st>>>(r,
+                                                                     status);
+  count_launch();
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decompress(const DecParams& p, int pairs, cudaStream_t st) {
-  return launch_dec(p, pairs, st);
+  return p.packed ? launch_dec_as<DecParams, 3>(p, pairs, st)
+         : p.wide ? launch_dec_as<DecParams, 2>(p, pairs, st)
+                  : launch_dec_as<DecParams, 0>(p, pairs, st);
 }
 
 cudaError_t launch_decompress_paged(const PagedParams& p, int pairs,
                                     cudaStream_t st) {
-  return launch_dec(p, pairs, st);
+  return p.wide ? launch_dec_as<PagedParams, 2>(p, pairs, st)
+                : launch_dec_as<PagedParams, 0>(p, pairs, st);
 }
 
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns,

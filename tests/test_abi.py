@@ -107,6 +107,8 @@ def test_null_handles_are_rejected(kv):
                               None, 0, None) == kv.KVTC_EINVAL
     assert L.kvtc_fields_unpack(None, 0, 1, 1, None, 0, None, 10, None, 0,
                                 None) == kv.KVTC_EINVAL
+    assert L.kvtc_decompress_packed(None, 0, 1, 1, None, 0, None, 10, arr,
+                                    128, None, None) == kv.KVTC_EINVAL
     L.kvtc_calib_free(None)  # no-op
 
 
