@@ -188,21 +188,24 @@ int kvtc_decompress_paged(const kvtc_calib* calib, int layer0, int nlayers,
  * there (technical summary 2B); this library runs a format of its own that
  * targets the one redundant part of a record, the high byte of each fp16
  * field.  Per stream and field slot (slot 2a = shift of active group a,
- * 2a + 1 = its scale), v = high byte >> 2 (sign and exponent) is stored as
- * v - vmin in dbits bits, vmin / dbits = the minimum and the bit length of
- * the range of v over the stream's records (dbits <= 6); the other bits are
- * kept, and the record's zero padding is dropped.
+ * 2a + 1 = its scale), v = high byte h >> 2 (sign and exponent) spans
+ * [vmin, vmin + 2^dbits) over the stream's records (dbits <= 6), so h is
+ * stored as h - 4 vmin in dbits + 2 bits; the other bits are kept, and the
+ * record's zero padding is dropped.
  *
  *   Packed stream (little-endian): header "KVFP", u32 T_c, u16 Rp (packed
  *   record bytes), u16 nslot (= 2 G_a), u32 0; slot table nslot x (u8 vmin,
- *   u8 dbits) zero-padded to 16-byte multiples; the s' + w' raw rows as in
- *   the codec stream; T_c packed records of Rp bytes; zeros to a 256-byte
- *   multiple.  Packed record: the low bytes of the 2 G_a fields in slot
- *   order; the codes, per slot v - vmin in dbits bits then the high byte's
- *   low 2 bits, least significant bit first, in 2 ceil(bits / 16) bytes;
- *   the bit-planes of the codec record unchanged.  Rp <= the record's used
- *   bytes, so a packed stream is never longer than the codec stream plus
- *   its header and table.  Streams are concatenated in (layer, K, V) order.
+ *   u8 dbits) zero-padded so that header and table fill 128 bytes (a
+ *   multiple of 128 above 56 slots); the s' + w' raw rows as in the codec
+ *   stream; T_c packed records of Rp bytes; zeros to a 256-byte multiple.
+ *   Packed record: the low bytes of the 2 G_a fields in slot order; the
+ *   codes, per slot h - 4 vmin in dbits + 2 bits, least significant bit
+ *   first, in 2 ceil(bits / 16) bytes; the bit-planes of the codec record
+ *   unchanged; zeros to a multiple of 4 bytes.  Rp <= R, so a packed
+ *   stream is never longer than the codec stream plus its 128-byte prefix.
+ *   The records of a stream start on a 128-byte line and 32 of them fill
+ *   whole lines, which the restore from packed input reads line by line.
+ *   Streams are concatenated in (layer, K, V) order.
  */
 
 /* Field packing holds one field slot per lane of a warp: every selected
@@ -274,9 +277,10 @@ int kvtc_fields_unpack(const kvtc_calib* calib, int layer0, int nlayers,
  * Each stream's header, slot table and length are checked against its
  * calibration, T, the offsets and src_bytes on the GPU before anything they
  * frame is read; a stream that does not match restores its coded tokens as
- * from all-zero records and flags KVTC_FLAG_FORMAT; its raw rows are copied
- * only when its magic, T_c and extent (both offsets on the 16-byte grid,
- * inside src_bytes) check out.
+ * from all-zero records and flags KVTC_FLAG_FORMAT.  Its raw rows are copied
+ * whenever its extent frames them (both offsets on the 16-byte grid, inside
+ * src_bytes), and, in a call with no coded token, only when its magic and
+ * T_c check out too; an out-of-frame stream flags KVTC_FLAG_FORMAT.
  * Kernel launches as for kvtc_decompress (the raw rows of a call with no
  * coded token take one copy launch per 96 streams).  Streams must keep at
  * most 15 groups, else ENOTSUP.  src 16-byte aligned, offsets 8.

@@ -48,7 +48,7 @@ constexpr int kFpBuf = kFpRawChunk;              // one input buffer
 constexpr int kFpSmem = 3 * kFpBuf + 256 + 16;   // 2 in, 1 out + padding
 
 __device__ __forceinline__ int fp_table_bytes(int ga) {
-  return (4 * ga + 15) & ~15;
+  return fp_prefix_bytes(ga) - kFpHeader;
 }
 __device__ __forceinline__ int64_t fp_align256(int64_t v) {
   return (v + 255) & ~int64_t(255);
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kFpLayoutThreads) fp_layout_kernel(
     }
     const FpSlots sl = fp_slots_from(vmin, d, nslot);
     const int hb2 = (sl.hbits + 15) >> 4;
-    const int rp = 2 * S.ga + 2 * hb2 + (S.used - 4 * S.ga);
+    const int rp = fp_record_bytes(S.ga, hb2, S.used);
     table[i][lane] = (uint16_t)(vmin | (d << 8));
     if (lane == 0)
       size[i] = fp_align256(kFpHeader + fp_table_bytes(S.ga) + S.raw_bytes +
@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kFpLayoutThreads) fp_layout_kernel(
 #pragma unroll
     for (int k = 16; k > 0; k >>= 1)
       hbits += __shfl_xor_sync(0xffffffffu, hbits, k);
-    const int rp = 2 * S.ga + 2 * ((hbits + 15) >> 4) + (S.used - 4 * S.ga);
+    const int rp = fp_record_bytes(S.ga, (hbits + 15) >> 4, S.used);
     if (lane == 0) {
       uint32_t* h = reinterpret_cast<uint32_t*>(o);
       h[0] = kFpMagic;
@@ -253,7 +253,8 @@ __global__ void __launch_bounds__(kFpLayoutThreads) fp_layout_kernel(
       if (p.first == 0 && i == 0) p.offsets[0] = 0;
     }
     uint16_t* t = reinterpret_cast<uint16_t*>(o + kFpHeader);
-    if (lane < tb / 2) t[lane] = lane < nslot ? table[i][lane] : 0;
+    for (int j = lane; j < tb / 2; j += 32)
+      t[j] = j < nslot ? table[i][j] : 0;
     if (S.tc == 0 && S.raw_bytes == 0) {  // nothing else: pad here
       const int64_t from = kFpHeader + tb;
       for (int64_t b = from + 4 * lane; b < size[i]; b += 128)
@@ -330,7 +331,7 @@ __global__ void __launch_bounds__(kFpThreads, 2) fp_tile_kernel(
         }
         const FpSlots sl = fp_slots_from(vmin, d, nslot);
         c_hb2 = (sl.hbits + 15) >> 4;
-        c_rp = 2 * ga + 2 * c_hb2 + (S.used - 4 * ga);
+        c_rp = fp_record_bytes(ga, c_hb2, S.used);
         if (!kPack) {
           const uint32_t* h = reinterpret_cast<const uint32_t*>(p.in + c_off);
           const uint32_t h0 = h[0], h1 = h[1], h2 = h[2];
@@ -491,7 +492,9 @@ __global__ void __launch_bounds__(kFpThreads, 2) fp_tile_kernel(
               s_out[(tok0 + u) * rp + lane] = (uint8_t)lo;
               const int v = (int)(hi >> 2) - sl.vmin;
               if (v < 0 || v > (int)umask) bad = true;
-              const uint32_t code = ((uint32_t)v & umask) | ((hi & 3u) << sl.d);
+              // h - 4 vmin: the low 2 bits of h, then v - vmin
+              const uint32_t code = (hi - 4u * (uint32_t)sl.vmin) &
+                                    ((4u << sl.d) - 1u);
               clo[u] = code << s5;
               chi[u] = s5 ? code >> (32 - s5) : 0u;
             }
@@ -526,11 +529,15 @@ __global__ void __launch_bounds__(kFpThreads, 2) fp_tile_kernel(
                 reinterpret_cast<uint16_t*>(
                     s_out + (tok0 + u) * rp)[ga + hb2 + j] = v[u];
           }
+          // the record's zero padding to a multiple of 4 bytes
+          if (lane < nt && 2 * (ga + hb2 + p2) < rp)
+            reinterpret_cast<uint16_t*>(s_out + (tok0 + lane) * rp)[ga + hb2 +
+                                                                    p2] = 0;
         }
       } else {
         const int R2 = R >> 1, u2 = used >> 1;
         const int k = sl.pos >> 4, sh = sl.pos & 15;
-        const uint32_t cmask = (4u << sl.d) - 1, umask = (1u << sl.d) - 1;
+        const uint32_t cmask = (4u << sl.d) - 1;
         for (int tok0 = 4 * warp; tok0 < ntok; tok0 += 4 * kFpWarps) {
           const int nt = min(4, ntok - tok0);
           uint32_t bits[4], lob[4];
@@ -548,8 +555,7 @@ __global__ void __launch_bounds__(kFpThreads, 2) fp_tile_kernel(
           for (int u = 0; u < 4; ++u) {
             if (u < nt && lane < nslot) {
               const uint32_t code = (bits[u] >> sh) & cmask;
-              const uint32_t hi =
-                  ((((code & umask) + sl.vmin) << 2) | (code >> sl.d)) & 0xffu;
+              const uint32_t hi = (code + 4u * (uint32_t)sl.vmin) & 0xffu;
               reinterpret_cast<uint16_t*>(s_out + (tok0 + u) * R)[lane] =
                   (uint16_t)(lob[u] | (hi << 8));
             }

@@ -437,10 +437,8 @@ int decompress_impl(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
       for (int k2 = 0; k2 < 2; ++k2) {
         if (rows[k2] <= 0) continue;
         if (packed) {
-          // the rows follow the header and the slot table (4 G_a bytes,
-          // padded to 16)
-          const int64_t at =
-              kFpHeader + ((4 * h.Ga + 15) & ~15) + (k2 ? s_ * rb : 0);
+          // the rows follow the header and the slot table
+          const int64_t at = fp_prefix_bytes(h.Ga) + (k2 ? s_ * rb : 0);
           if (!raw_list_add_packed(p->raw, (int)i, (int)tc, at, d2[k2],
                                    2 * ld, rows[k2], rb))
             ret = KVTC_EINVAL;
@@ -1093,15 +1091,13 @@ int record_used(const HostStream& h) {
   return u;
 }
 
-int64_t fp_table_bytes_host(int ga) { return align_up(4LL * ga, 16); }
-
 // Worst-case packed bytes of one stream (every slot needing 6 offset bits
-// gives Rp = used bytes).
+// gives the longest packed record: the used bytes, padded to 4).
 int64_t fp_bound_of(const kvtc_calib* c, const HostStream& h, int64_t T) {
   int64_t s_, w_, tc;
   split_tokens(T, c->sink, c->window, &s_, &w_, &tc);
-  return align_up(kFpHeader + fp_table_bytes_host(h.Ga) +
-                      (s_ + w_) * h.D * 2 + tc * record_used(h),
+  return align_up(fp_prefix_bytes(h.Ga) + (s_ + w_) * h.D * 2 +
+                      tc * align_up(record_used(h), 4),
                   256);
 }
 

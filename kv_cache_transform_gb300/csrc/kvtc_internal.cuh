@@ -196,6 +196,17 @@ constexpr int kFpRawChunk = 32768;    // raw-row bytes per copy item; a
                                       // record tile is at most this long
 constexpr int kFpHeader = 16;         // packed stream header bytes
 constexpr uint32_t kFpMagic = 0x5046564Bu;  // "KVFP", little-endian
+// Bytes of a packed stream's header and slot table: a multiple of 128, so
+// that its records start on a 128-byte line of the stream.
+__host__ __device__ __forceinline__ int fp_prefix_bytes(int ga) {
+  return (kFpHeader + 4 * ga + 127) & ~127;
+}
+// Packed record bytes: 2 G_a low bytes, 2 hb2 code bytes, the bit-planes
+// (used - 4 G_a bytes), zero-padded to a multiple of 4.
+__host__ __device__ __forceinline__ int fp_record_bytes(int ga, int hb2,
+                                                        int used) {
+  return (2 * hb2 + used - 2 * ga + 3) & ~3;
+}
 struct FpStream {
   int64_t in_off;       // pack: codec stream offset in the input
   int64_t out_off;      // unpack: codec stream offset in the output

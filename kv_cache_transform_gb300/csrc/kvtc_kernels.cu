@@ -171,8 +171,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 // 16-byte chunks by the `stride` threads of the raw-copy role across the
 // grid (thread `tid` of them), four chunks in flight per thread.  Runs
 // beside the tensor-core work of the same kernel.  kPk: segments may sit in
-// packed streams (restore from packed input).
-template <bool kPk = false>
+// packed streams (restore from packed input), read where the stream's
+// offsets frame them; kHdr: and only when the stream's header holds the
+// magic and T_c (in the restore kernel the prologue checks the header of
+// every stream, as it has coded tokens, so the copy skips that read).
+template <bool kPk = false, bool kHdr = false>
 __device__ __forceinline__ void raw_list_copy(const RawList& r, int64_t tid,
                                               int64_t stride,
                                               unsigned* status) {
@@ -203,7 +206,8 @@ __device__ __forceinline__ void raw_list_copy(const RawList& r, int64_t tid,
               o1 <= r.pk_bytes) {
             const uint32_t* hd =
                 reinterpret_cast<const uint32_t*>(r.pk_base + o0);
-            if (__ldg(hd) == kFpMagic && (int32_t)__ldg(hd + 1) == g.pk_tc)
+            if (!kHdr ||
+                (__ldg(hd) == kFpMagic && (int32_t)__ldg(hd + 1) == g.pk_tc))
               src = reinterpret_cast<const char*>(r.pk_base) + o0 + g.pk_off;
           }
           if (!src) {
@@ -225,8 +229,8 @@ __device__ __forceinline__ void raw_list_copy(const RawList& r, int64_t tid,
 // its own, every thread of the grid one copier.
 __global__ void __launch_bounds__(256)
     raw_list_kernel(const __grid_constant__ RawList r, unsigned* status) {
-  raw_list_copy<true>(r, (int64_t)blockIdx.x * 256 + threadIdx.x,
-                      (int64_t)gridDim.x * 256, status);
+  raw_list_copy<true, true>(r, (int64_t)blockIdx.x * 256 + threadIdx.x,
+                            (int64_t)gridDim.x * 256, status);
 }
 
 // ======================================================================
@@ -548,6 +552,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
     const uint32_t a_full_leader = mapa_shared(smem_u32(a_full), 0);
     uint32_t it = 0;
     bool ok = true;
+    // Packed input: the offsets, header and slot table of the set's next
+    // tile are loaded while this one is decoded (registers; an offset of -1
+    // marks a stream whose offsets do not frame its header and table), so
+    // each tile waits on memory once, for its records.
+    int64_t nx_o0 = -1, nx_o1 = 0;
+    uint32_t nx_hw = 0;
+    const auto pk_fetch = [&](int itm) {
+      nx_o0 = -1;
+      nx_o1 = 0;
+      nx_hw = 0;
+      if constexpr (kPacked) {
+      if (itm >= total) return;
+      const int sg = itm / p.tiles_per_seg;
+      const int gn = p.streams[p.seg[sg].cs].Ga;
+      const int64_t a0 = p.raw.pk_offs[sg + p.pk_first];
+      const int64_t a1 = p.raw.pk_offs[sg + p.pk_first + 1];
+      if (a0 >= 0 && ((a0 | a1) & 15) == 0 && a1 >= a0 + fp_prefix_bytes(gn) &&
+          a1 <= p.raw.pk_bytes) {
+        nx_o0 = a0;
+        nx_o1 = a1;
+        // the 128-byte prefix (header, slot table) in one load, a word a
+        // lane; the slot entries are unpacked when the tile starts
+        nx_hw = __ldg(reinterpret_cast<const uint32_t*>(p.raw.pk_base + a0) +
+                      lane);
+      }
+      }
+    };
+    if constexpr (kPacked) pk_fetch(pair + (int)set * npairs);
     KVTC_TR_DECL
     for (int item = pair; item < total; item += npairs, ++it) {
       // A buffers: two of 128 columns, each filled by its own set of warps
@@ -579,20 +611,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       // against the calibration, T and the offsets before anything they
       // frame is read; its records are Rp bytes long.
       int pk_vmin = 0, pk_d = 0, pk_pos = 0, pk_hb2 = 0, pk_rp = 0;
+      int pk_po = 0;
+      uint32_t pk_grp = 0;
       bool pk_ok = false;
       if constexpr (kPacked) {
-        const int si = t.seg + p.pk_first, ns = 2 * Ga;
-        const int64_t o0 = p.raw.pk_offs[si], o1 = p.raw.pk_offs[si + 1];
-        const int tb = (4 * Ga + 15) & ~15;
+        const int ns = 2 * Ga;
+        const int64_t o0 = nx_o0, o1 = nx_o1;   // fetched for this tile
+        const uint32_t hw = nx_hw;              // prefix word `lane`
+        // slot `lane`'s entry: halfword lane of the table (word 4 + lane/2)
+        const uint32_t tw = __shfl_sync(0xFFFFFFFFu, hw, (4 + (lane >> 1)) & 31);
+        const uint32_t te = lane < ns ? (tw >> ((lane & 1) << 4)) & 0xFFFFu : 0u;
+        const int pre = fp_prefix_bytes(Ga);  // header + slot table
         const int64_t rawb = (int64_t)p.pk_raw_rows * ds->D * 2;
-        const bool in = o0 >= 0 && (o0 & 15) == 0 && (o1 & 15) == 0 &&
-                        o1 >= o0 + kFpHeader + tb && o1 <= p.raw.pk_bytes;
+        const bool in = o0 >= 0;
         const uint8_t* sb = p.raw.pk_base + (in ? o0 : 0);
-        uint32_t hw = 0, te = 0;
-        if (in && lane < 4)
-          hw = __ldg(reinterpret_cast<const uint32_t*>(sb) + lane);
-        if (in && lane < ns)
-          te = __ldg(reinterpret_cast<const uint16_t*>(sb + kFpHeader) + lane);
         pk_vmin = (int)(te & 0xFFu);
         pk_d = (int)(te >> 8);
         const int wbits = lane < ns ? pk_d + 2 : 0;
@@ -606,7 +638,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         pk_hb2 = (__shfl_sync(0xFFFFFFFFu, incl, 31) + 15) >> 4;
         const int used = __shfl_sync(0xFFFFFFFFu, my_po, Ga - 1) +
                          2 * __shfl_sync(0xFFFFFFFFu, my_b, Ga - 1);
-        pk_rp = used - 2 * Ga + 2 * pk_hb2;
+        pk_rp = fp_record_bytes(Ga, pk_hb2, used);
         const uint32_t h0 = __shfl_sync(0xFFFFFFFFu, hw, 0);
         const uint32_t h1 = __shfl_sync(0xFFFFFFFFu, hw, 1);
         const uint32_t h2 = __shfl_sync(0xFFFFFFFFu, hw, 2);
@@ -614,20 +646,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         pk_ok = __all_sync(0xFFFFFFFFu, slot_ok) && in && h0 == kFpMagic &&
                 (int)h1 == t.tc && (int)(h2 & 0xFFFFu) == pk_rp &&
                 (int)(h2 >> 16) == ns &&
-                o0 + kFpHeader + tb + rawb + (int64_t)t.tc * pk_rp <= o1;
+                o0 + pre + rawb + (int64_t)t.tc * pk_rp <= o1;
         if (!pk_ok) {
           // decoded as all-zero records: zero fields, codes and planes
           pk_vmin = pk_d = pk_pos = pk_hb2 = 0;
           if (lane == 0 && q == 0 && rank == 0)
             atomicOr(p.status, KVTC_FLAG_FORMAT);
         }
-        rbase = sb + kFpHeader + tb + rawb + (int64_t)row0 * pk_rp;
+        rbase = sb + pre + rawb + (int64_t)row0 * pk_rp;
+        // lane a (< Ga): group a's two slots in one word -- the bit where
+        // slot 2a's code starts (the codes begin at halfword Ga), the two
+        // code widths less 2 and the two 4 vmin
+        const int v0 = __shfl_sync(0xFFFFFFFFu, pk_vmin, (2 * lane) & 31);
+        const int v1 = __shfl_sync(0xFFFFFFFFu, pk_vmin, (2 * lane + 1) & 31);
+        const int d0 = __shfl_sync(0xFFFFFFFFu, pk_d, (2 * lane) & 31);
+        const int d1 = __shfl_sync(0xFFFFFFFFu, pk_d, (2 * lane + 1) & 31);
+        const int bp = 16 * Ga + __shfl_sync(0xFFFFFFFFu, pk_pos,
+                                             (2 * lane) & 31);
+        pk_grp = (uint32_t)bp | ((uint32_t)d0 << 10) | ((uint32_t)d1 << 13) |
+                 ((uint32_t)(v0 & 63) << 18) | ((uint32_t)(v1 & 63) << 26);
+        pk_po = my_po - 2 * Ga + 2 * pk_hb2;  // planes follow the codes
       }
       if constexpr (kPacked) {
-        // the warp's packed records are 32 Rp contiguous bytes (16-byte
-        // aligned: Rp is even and the stream's regions are multiples of
-        // 16); coalesced 16-byte loads, each halfword stored at its token's
-        // place in the word-transposed staging
+        // the warp's packed records are 32 Rp contiguous bytes (whole
+        // 128-byte lines of the stream: Rp is a multiple of 4 and the
+        // records start on a line); coalesced 16-byte loads, each word
+        // stored at its token's place in the word-transposed staging
         const int nvalid = pk_ok ? min(max(t.tc - row0, 0), 32) : 0;
         // tokens without a record (past T_c, or all of an invalid stream)
         // decode from zeros, as in the codec layout
@@ -636,9 +680,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
           for (int i = lane; i < rec_words * nz; i += 32)
             stg[(i / nz) * 33 + nvalid + i % nz] = 0u;
         }
-        const int hpr = pk_rp >> 1;
+        const int wpr = pk_rp >> 2;
         const int nchunk = (nvalid * pk_rp + 15) >> 4;
-        const uint32_t stg_a = smem_u32(stg);
         for (int c0 = 0; c0 < nchunk; c0 += 8 * 32) {
           uint4 v[8];
 #pragma unroll
@@ -650,24 +693,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int c = c0 + u * 32 + lane;
-            if (c < nchunk) {
-              const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-              int tr = (8 * c) / hpr;
-              int idx = 8 * c - tr * hpr;
+            if (c >= nchunk) continue;
+            const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            int tr = (4 * c) / wpr;
+            int wd = 4 * c - tr * wpr;
 #pragma unroll
-              for (int h = 0; h < 8; ++h) {
-                if (tr < nvalid)
-                  sts_u16(stg_a + (uint32_t)((((idx >> 1) * 33 + tr) << 2) +
-                                             ((idx & 1) << 1)),
-                          (wv[h >> 1] >> ((h & 1) << 4)) & 0xFFFFu);
-                if (++idx == hpr) {
-                  idx = 0;
-                  ++tr;
-                }
+            for (int j = 0; j < 4; ++j) {
+              if (tr < nvalid) stg[wd * 33 + tr] = wv[j];
+              if (++wd == wpr) {
+                wd = 0;
+                ++tr;
               }
             }
           }
         }
+        pk_fetch(item + 2 * npairs);  // the set's next tile
       } else {
       // Coalesced 16-byte loads of the warp's 32 records (up to eight in
       // flight per lane), stored word-transposed ([word][token], row pitch
@@ -709,32 +749,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
           tmem + ((uint32_t)(q * 32) << 16) + 256u + abuf * 128u;
       for (int a = 0; a < Ga; ++a) {
         const int b = __shfl_sync(0xFFFFFFFFu, my_b, a);
-        int po = __shfl_sync(0xFFFFFFFFu, my_po, a);
+        int po;
         uint32_t f;
         if constexpr (kPacked) {
           // packed record: the low bytes of the 2 Ga fields, the codes of
           // their high bytes (per slot, v - vmin in d bits, then the high
           // byte's low two bits), the bit-planes
-          const auto hword = [&](int i) -> uint32_t {
-            return i < rec_words * 2
-                       ? (stg[(i >> 1) * 33 + lane] >> ((i & 1) << 4)) & 0xFFFFu
-                       : 0u;
-          };
-          const auto high = [&](int sl) -> uint32_t {
-            const int vmin = __shfl_sync(0xFFFFFFFFu, pk_vmin, sl);
-            const int d = __shfl_sync(0xFFFFFFFFu, pk_d, sl);
-            const int pos = __shfl_sync(0xFFFFFFFFu, pk_pos, sl);
-            const int i = Ga + (pos >> 4);
-            const uint32_t bits = hword(i) | (hword(i + 1) << 16);
-            const uint32_t code = (bits >> (pos & 15)) & ((4u << d) - 1u);
-            return ((((code & ((1u << d) - 1u)) + (uint32_t)vmin) << 2) |
-                    (code >> d)) & 0xFFu;
-          };
-          const uint32_t lo16 = hword(a);
-          f = (lo16 & 0xFFu) | (high(2 * a) << 8) | ((lo16 >> 8) << 16) |
-              (high(2 * a + 1) << 24);
-          po = po - 2 * Ga + 2 * pk_hb2;  // planes follow the codes
+          po = __shfl_sync(0xFFFFFFFFu, pk_po, a);
+          const uint32_t e = __shfl_sync(0xFFFFFFFFu, pk_grp, a);
+          const uint32_t wi = min((e & 1023u) >> 5, (uint32_t)rec_words - 2u);
+          const uint32_t bits = __funnelshift_r(
+              stg[wi * 33 + lane], stg[(wi + 1) * 33 + lane], e & 31u);
+          // code = high byte - 4 vmin, in d + 2 bits
+          const uint32_t d0 = (e >> 10) & 7u, d1 = (e >> 13) & 7u;
+          const uint32_t c0 = bits & ((4u << d0) - 1u);
+          const uint32_t c1 = (bits >> (d0 + 2u)) & ((4u << d1) - 1u);
+          const uint32_t h0 = (c0 + ((e >> 16) & 0xFCu)) & 0xFFu;
+          const uint32_t h1 = (c1 + ((e >> 24) & 0xFCu)) & 0xFFu;
+          const uint32_t lo16 = stg[(a >> 1) * 33 + lane] >> ((a & 1) << 4);
+          // shift = lo byte 0 | h0 << 8, scale = lo byte 1 | h1 << 8
+          f = __byte_perm(lo16, h0 | (h1 << 8), 0x5140);
         } else {
+          po = __shfl_sync(0xFFFFFFFFu, my_po, a);
           f = stg[a * 33 + lane];
         }
         uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;

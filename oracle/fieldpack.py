@@ -14,8 +14,8 @@ record's zero padding is dropped.
 Packed stream of one (layer, K|V), little-endian:
   header      b"KVFP", u32 T_c, u16 Rp (packed record bytes),
               u16 nslot (= 2 G_a), u32 0                          16 bytes
-  slot table  per slot s: u8 vmin_s, u8 dbits_s; zero-padded to a multiple
-              of 16 bytes
+  slot table  per slot s: u8 vmin_s, u8 dbits_s; zero-padded so that
+              header and table together fill a multiple of 128 bytes
   raw rows    the sink and window rows, unchanged ((s'+w') x 2D bytes)
   records     T_c packed records of Rp bytes
   padding     zeros to a multiple of 256 bytes
@@ -26,13 +26,19 @@ slot s over the stream's tokens and dbits_s the bit length of
 vmax_s - vmin_s (0 when T_c = 0).
 Packed record of one token:
   the low bytes of its fields in slot order                       2 G_a B
-  the high-byte codes: for s = 0 .. nslot - 1, v - vmin_s in dbits_s bits,
-  then h & 3 in 2 bits, packed least significant bit first into
-  2 ceil(sum_s (dbits_s + 2) / 16) bytes (unused high bits zero)
+  the high-byte codes: for s = 0 .. nslot - 1, h - 4 vmin_s in
+  dbits_s + 2 bits (its low 2 bits are h & 3, the others v - vmin_s),
+  packed least significant bit first into 2 ceil(sum_s (dbits_s + 2) / 16)
+  bytes (unused high bits zero)
   the bit-planes, record bytes [4 G_a, used)
+  zero bytes to a multiple of 4
 Every part has an even number of bytes, so a packed record keeps the
-16-bit alignment of the bit-planes; Rp never exceeds the used bytes of a
-record (dbits_s <= 6, so the codes take at most 16 G_a bits).
+16-bit alignment of the bit-planes, and its length is a multiple of 4.
+Before that last padding it never exceeds the used bytes of a record
+(dbits_s <= 6, so the codes take at most 16 G_a bits), so Rp <= R.  The
+128-byte prefix and the 4-byte record length are layout choices of this
+format: a stream's records start on a 128-byte boundary of the stream and
+32 consecutive records span whole 128-byte lines.
 """
 from __future__ import annotations
 
@@ -76,7 +82,8 @@ def code_bytes(dbits: np.ndarray) -> int:
 def packed_record_bytes(bits: np.ndarray, dbits: np.ndarray) -> int:
     ga = len(bits)
     _, _, used = codec.record_layout(bits)
-    return 2 * ga + code_bytes(dbits) + (used - 4 * ga)
+    n = 2 * ga + code_bytes(dbits) + (used - 4 * ga)
+    return -(-n // 4) * 4
 
 
 def pack_records(records: np.ndarray, bits: np.ndarray):
@@ -94,19 +101,17 @@ def pack_records(records: np.ndarray, bits: np.ndarray):
     # code bits of every token, least significant first, slot after slot
     cols = []
     for s in range(2 * ga):
-        u = (hi[:, s].astype(np.int64) >> 2) - vmin[s]
-        for b in range(int(dbits[s])):
-            cols.append((u >> b) & 1)
-        m2 = hi[:, s].astype(np.int64) & 3
-        cols.append(m2 & 1)
-        cols.append((m2 >> 1) & 1)
+        c = hi[:, s].astype(np.int64) - 4 * vmin[s]
+        for b in range(int(dbits[s]) + 2):
+            cols.append((c >> b) & 1)
     hbytes = code_bytes(dbits)
     bitmat = np.zeros((n, 8 * hbytes), dtype=np.uint8)
     if cols:
         bitmat[:, :len(cols)] = np.stack(cols, axis=1)
     hb = np.packbits(bitmat, axis=1, bitorder="little")
     out[:, 2 * ga:2 * ga + hbytes] = hb
-    out[:, 2 * ga + hbytes:] = records[:, 4 * ga:used]
+    out[:, 2 * ga + hbytes:2 * ga + hbytes + used - 4 * ga] = \
+        records[:, 4 * ga:used]
     return vmin, dbits, out
 
 
@@ -125,22 +130,22 @@ def unpack_records(packed: np.ndarray, bits: np.ndarray, vmin: np.ndarray,
                            bitorder="little")[:, :hbits].astype(np.int64)
     pos = 0
     for s in range(2 * ga):
-        u = np.zeros(n, dtype=np.int64)
-        for b in range(int(dbits[s])):
-            u |= bitmat[:, pos] << b
+        c = np.zeros(n, dtype=np.int64)
+        for b in range(int(dbits[s]) + 2):
+            c |= bitmat[:, pos] << b
             pos += 1
-        m2 = bitmat[:, pos] | (bitmat[:, pos + 1] << 1)
-        pos += 2
-        h = ((u + vmin[s]) << 2) | m2
+        h = c + 4 * vmin[s]
         a, which = divmod(s, 2)
         rec[:, 4 * a + 2 * which + 1] = h.astype(np.uint8)
         rec[:, 4 * a + 2 * which] = packed[:, s]
-    rec[:, 4 * ga:used] = packed[:, 2 * ga + hbytes:]
+    rec[:, 4 * ga:used] = \
+        packed[:, 2 * ga + hbytes:2 * ga + hbytes + used - 4 * ga]
     return rec
 
 
 def _table_bytes(nslot: int) -> int:
-    return -(-2 * nslot // 16) * 16
+    """Slot table bytes: header and table fill a multiple of 128 bytes."""
+    return -(-(HEADER + 2 * nslot) // 128) * 128 - HEADER
 
 
 def pack_stream(buf: bytes, T: int, sc: codec.StreamCalib) -> bytes:

@@ -196,8 +196,8 @@ def zero_records(cb: bytes, T: int, sc) -> bytes:
 def test_corrupt_packed_streams_are_flagged(kv, torch):
     """A packed stream whose header, slot table or extent does not match is
     flagged KVTC_FLAG_FORMAT without a fault: its coded tokens restore as
-    from all-zero records; its raw rows are copied only when its magic, T_c
-    and extent check out; the other stream restores as from intact input."""
+    from all-zero records; its raw rows are copied whenever its extent
+    frames them; the other stream restores as from intact input."""
     name, streams, T = "edge_d192", [(0, 0), (0, 1)], 300
     w = synth.WORKLOADS[name]
     blob, scs = workload_calib(name, streams)
@@ -245,10 +245,10 @@ def test_corrupt_packed_streams_are_flagged(kv, torch):
             np.testing.assert_array_equal(got, want)
 
     good = np.array([0, n0, n0 + n1], dtype=np.int64)
-    for at, raw_kept in ((0, False), (4, False), (8, True), (10, True)):
-        bad = [bytearray(p) for p in pbs]   # magic, T_c, Rp, slot count
+    for at in (0, 4, 8, 10):                # magic, T_c, Rp, slot count
+        bad = [bytearray(p) for p in pbs]
         bad[0][at] ^= 1
-        check(bad, good, 0, raw_kept)
+        check(bad, good, 0, True)
     bad = [bytearray(p) for p in pbs]
     bad[1][16 + 1] = 7                      # a slot's dbits above 6
     check(bad, good, 1, True)
@@ -258,6 +258,32 @@ def test_corrupt_packed_streams_are_flagged(kv, torch):
     # an offset off the 16-byte grid: the end of stream 0 and the start of
     # stream 1, both flagged
     check(pbs, np.array([0, n0 + 8, n0 + n1], dtype=np.int64), (0, 1), False)
+    calib.free()
+
+
+def test_no_coded_token_checks_the_header(kv, torch):
+    """T = 12 (sink 4 + 8 window rows, no record): the raw rows come back
+    through the copy launch, which also checks magic and T_c; a stream whose
+    T_c is wrong is flagged and left untouched, the other restored."""
+    name, streams, T = "edge_d192", [(0, 0), (0, 1)], 12
+    w = synth.WORKLOADS[name]
+    blob, scs = workload_calib(name, streams)
+    calib = kv.kvtc_calib_load(blob, 0)
+    D = w.D
+    cbs = [codec.compress_stream(synth.eval_tokens(w, l, k, T=T),
+                                 scs[(l, k)][0]) for l, k in streams]
+    pbs = [bytearray(fieldpack.pack_stream(b, T, scs[s][0]))
+           for b, s in zip(cbs, streams)]
+    pbs[1][4] ^= 1
+    pb = b"".join(bytes(p) for p in pbs)
+    offs = np.array([0, len(pbs[0]), len(pb)], dtype=np.int64)
+    out = outputs(torch, 2, T, D)
+    kv.kvtc_decompress_packed(calib, 0, 1, 3, dev_bytes(torch, pb), len(pb),
+                              torch.from_numpy(offs).cuda(), T, out, D)
+    assert kv.kvtc_device_status(calib) == kv.KVTC_FLAG_FORMAT
+    x0 = synth.eval_tokens(w, 0, 0, T=T)
+    np.testing.assert_array_equal(out[0].cpu().numpy().view(np.uint16), x0)
+    assert np.all(out[1].cpu().numpy().view(np.uint16) == NAN_BF16)
     calib.free()
 
 

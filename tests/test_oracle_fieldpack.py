@@ -55,7 +55,9 @@ def test_golden_example_stream():
 
 
 def _brute_codes(rec_row, bits, vmin, dbits):
-    """Code bytes of one token built as a string of '0'/'1' characters."""
+    """Code bytes of one token built as a string of '0'/'1' characters:
+    per slot the two low bits of the high byte, then its sign/exponent
+    offset from the slot's minimum, least significant bit first."""
     ga = len(bits)
     s = ""
     for a in range(ga):
@@ -65,9 +67,9 @@ def _brute_codes(rec_row, bits, vmin, dbits):
             u = h // 4 - int(vmin[slot])
             assert 0 <= u < 2 ** int(dbits[slot]) or (u == 0 and
                                                       dbits[slot] == 0)
+            s += format(h % 4, "02b")[::-1]
             s += format(u, "b").zfill(int(dbits[slot]))[::-1] \
                 if dbits[slot] else ""
-            s += format(h % 4, "02b")[::-1]
     while len(s) % 16:
         s += "0"
     return bytes(int(s[i:i + 8][::-1], 2) for i in range(0, len(s), 8))
@@ -104,7 +106,8 @@ def test_brute_force_codes_and_layout(seed):
             assert vmin[s] == col.min()
             assert dbits[s] == int(col.max() - col.min()).bit_length()
         hb = len(_brute_codes(rec[0], bits, vmin, dbits))
-        assert packed.shape[1] == 2 * ga + hb + used - 4 * ga
+        body = 2 * ga + hb + used - 4 * ga
+        assert packed.shape[1] == body + (-body) % 4
         for t in range(n):
             row = packed[t]
             lo = bytes(rec[t, [4 * (s // 2) + 2 * (s % 2)
@@ -112,12 +115,14 @@ def test_brute_force_codes_and_layout(seed):
             assert row[:2 * ga].tobytes() == lo
             assert row[2 * ga:2 * ga + hb].tobytes() == \
                 _brute_codes(rec[t], bits, vmin, dbits)
-            assert row[2 * ga + hb:].tobytes() == rec[t, 4 * ga:used].tobytes()
+            assert row[2 * ga + hb:body].tobytes() == \
+                rec[t, 4 * ga:used].tobytes()
+            assert not row[body:].any()
         back = fieldpack.unpack_records(packed, bits, vmin, dbits, R)
         np.testing.assert_array_equal(back, rec)
 
 
-def test_packed_record_never_larger_and_even():
+def test_packed_record_never_larger_and_word_sized():
     rng = np.random.default_rng(11)
     for _ in range(200):
         ga = int(rng.integers(1, 16))
@@ -125,11 +130,14 @@ def test_packed_record_never_larger_and_even():
         dbits = rng.integers(0, 7, 2 * ga)
         _, _, used = codec.record_layout(bits)
         rp = fieldpack.packed_record_bytes(bits, dbits)
-        assert rp % 2 == 0 and rp <= used
-    # worst case: every slot's sign/exponent spans all 64 values
+        assert rp % 4 == 0 and rp <= used + (-used) % 4
+        assert rp <= 16 * -(-used // 16)           # never longer than R
+    # worst case: every slot's sign/exponent spans all 64 values; used is
+    # 4 * 3 + 2 * 6 = 24 bytes
     bits = np.array([1, 2, 3])
-    assert fieldpack.packed_record_bytes(bits, np.full(6, 6)) == \
-        codec.record_layout(bits)[2]
+    assert fieldpack.packed_record_bytes(bits, np.full(6, 6)) == 24
+    # used = 4 + 2 = 6 bytes, codes of 2 slots x 8 bits: 2 + 2 + 2 -> 8
+    assert fieldpack.packed_record_bytes(np.array([1]), np.full(2, 6)) == 8
 
 
 def test_constant_fields_cost_two_bits_per_slot():
@@ -139,7 +147,7 @@ def test_constant_fields_cost_two_bits_per_slot():
     _, dbits, packed = fieldpack.pack_records(rec, bits)
     assert dbits.sum() == 0
     assert fieldpack.code_bytes(dbits) == 2   # 8 slots x 2 bits
-    assert packed.shape[1] == 8 + 2 + 16
+    assert packed.shape[1] == 8 + 2 + 16 + 2  # padded to a multiple of 4
 
 
 @pytest.fixture(scope="module")
@@ -164,7 +172,8 @@ def test_stream_round_trip_is_lossless(tiny_sc, T):
     assert len(pbuf) == fieldpack.packed_stream_bytes(T, sc, rp)
     assert fieldpack.unpack_stream(pbuf, T, sc) == buf
     s_, w_, tc = codec.split_tokens(T, sc.sink, sc.window)
-    off = fieldpack.HEADER + 16 * -(-4 * len(sc.bits) // 16)
+    off = 128 * -(-(16 + 4 * len(sc.bits)) // 128)   # header + table
+    assert off % 128 == 0
     assert pbuf[off:off + (s_ + w_) * sc.D * 2] == buf[:(s_ + w_) * sc.D * 2]
 
 
