@@ -98,13 +98,13 @@ typedef struct kvtc_calib kvtc_calib;
  * fp32 mu and fp32 m = bf16(V_kept) mu, group layout tables, TMA
  * descriptors.  Requirements: D % 64 == 0, D <= 8192, 16 <= k <= 496 (the
  * reconstruction holds k plus one mean step of 16 fp16 columns in 256
- * tensor-memory columns), record bytes <= 256, and the projection's
- * two-stage shared-memory ring fits beside its record staging
- * (2 (32768 + 128 k) + 264 R + 1344 <= 232448 bytes, R the record bytes);
- * otherwise ENOTSUP.  Up to k = 240 both kernels double-buffer their
- * tensor-memory operands; above, a launch that holds such a stream
- * single-buffers them (the projection above k = 256, the reconstruction's
- * A operand above k = 240).
+ * tensor-memory columns) and record bytes <= 256; otherwise ENOTSUP.  Up
+ * to k = 240 both kernels double-buffer their tensor-memory operands;
+ * above, a launch that holds such a stream single-buffers them (the
+ * projection above k = 256, the reconstruction's A operand above k = 240).
+ * The projection's shared-memory ring holds two or more stages while
+ * 2 (32768 + 128 k) + 264 R + 1344 <= 232448 bytes (k <= 382 at R = 256),
+ * one stage beyond.
  * Errors: EINVAL, EFORMAT, ENOMEM, ECUDA, ENOTSUP.
  */
 int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,

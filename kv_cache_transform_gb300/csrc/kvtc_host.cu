@@ -625,10 +625,11 @@ int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
     }
     h.Ga = ga;
     h.R = R;
-    // the projection's two-stage ring (x tile and this CTA's V_enc half,
-    // two K blocks each) and its record staging must fit shared memory
+    // the projection's ring (at least one stage: x tile and this CTA's
+    // V_enc half, two K blocks each) and its record staging must fit shared
+    // memory (always so for k <= 496 and R <= 256)
     const bool smem_ok =
-        compress_smem_bytes(2, 2 * kTileM * 128 + h.k * 128, R / 4) <= 232448;
+        compress_smem_bytes(1, 2 * kTileM * 128 + h.k * 128, R / 4) <= 232448;
     if (h.D % 64 || h.D > kMaxD || h.k > kMaxK || h.k == 0 || R > kMaxRecord ||
         !smem_ok || find_stream(c, h.layer, h.kv) >= 0) {
       status = find_stream(c, h.layer, h.kv) >= 0 ? KVTC_EFORMAT : KVTC_ENOTSUP;
@@ -940,8 +941,11 @@ int kvtc_compress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
     p->b_bytes_max = 2 * kmax * 64;
     p->stage_bytes = 2 * kTileM * 128 + p->b_bytes_max;
     p->rec_stg_words = rmax / 4;
+    // the deepest ring that fits: two stages or more up to k = 382 at
+    // 256-byte records, one beyond (the load of the next K blocks then
+    // waits for the MMAs on this stage)
     int nst = 6;
-    while (nst > 2 && compress_smem_bytes(nst, p->stage_bytes,
+    while (nst > 1 && compress_smem_bytes(nst, p->stage_bytes,
                                           p->rec_stg_words) > 232448)
       --nst;
     p->nstages = nst;

@@ -107,6 +107,18 @@ WORKLOADS = {
                                    tokens=8192, requests=1, rank=1024,
                                    spectrum_p=0.0, outliers=False, sink=4,
                                    window=128, avg_bits=1.0),
+    # cross-layer basis: each stream is two consecutive layers of the
+    # config-2 shape, a token's rows of layers 2l and 2l + 1 side by side
+    # (D = 2 x 8 x 128 = 2048, "layer" l of this workload = that pair), one
+    # basis over the pair.  The two layers share their latent factors (rank
+    # 128 over the 2048-wide row), the similarity across layers a shared
+    # basis relies on; 1 bit per coefficient, as the per-layer workload
+    # (256-byte records)
+    "llama31_8b_8k_xlayer2": Workload("llama31_8b_8k_xlayer2", layers=16,
+                                      kv=(0, 1), heads=16, head_dim=128,
+                                      tokens=8192, requests=1, rank=128,
+                                      spectrum_p=1.0, outliers=True, sink=4,
+                                      window=128, avg_bits=1.0),
     "mistral_nemo_12b_32k": Workload("mistral_nemo_12b_32k", layers=40,
                                      kv=(0, 1), heads=8, head_dim=128,
                                      tokens=32768, requests=1, rank=128,

@@ -124,9 +124,8 @@ def test_kept_components_beyond_the_kernel_limits_are_refused(kv):
     - k = 512 (every group of a D = 512 stream at width 1): the
       reconstruction holds k plus one mean step of 16 fp16 columns in 256
       TMEM columns, so k <= 496;
-    - k = 400 with 256-byte records: the projection's two-stage ring (x and
-      this CTA's 200 V_enc rows, two K blocks each) and the record staging
-      exceed shared memory."""
+    - records over 256 bytes (a budget of 2064 bits: R = 272), longer than
+      the kernels' record staging takes."""
     D = 512
     widths = np.ones(D // 16, dtype=np.uint8)
     blob = calibrate.write_blob(
@@ -136,5 +135,5 @@ def test_kept_components_beyond_the_kernel_limits_are_refused(kv):
     widths = np.zeros(D // 16, dtype=np.uint8)
     widths[:25] = 2
     blob = calibrate.write_blob(
-        [(0, 0, np.zeros(D), np.eye(D), np.ones(D), widths)], 4, 16, 2048)
+        [(0, 0, np.zeros(D), np.eye(D), np.ones(D), widths)], 4, 16, 2064)
     assert load_raw(kv, blob) == kv.KVTC_ENOTSUP

@@ -139,6 +139,12 @@ def test_full_llama31_8b_8k_k336_sampled(kv, torch):
                    tag=f"{name}, 21 one-bit groups (k = 336)")
 
 
+def test_full_cross_layer_pairs_sampled(kv, torch):
+    """Cross-layer basis over layer pairs: 32 streams x 8192 tokens of
+    D = 2048 (1.07 GB raw), k = 480, 256-byte records."""
+    run_contiguous(kv, torch, "llama31_8b_8k_xlayer2", (0, 1, 17, 30, 31))
+
+
 def test_full_mistral_nemo_12b_32k_sampled(kv, torch):
     """80 streams x 32768 tokens (5.4 GB raw), k = 112, 64-byte records."""
     run_contiguous(kv, torch, "mistral_nemo_12b_32k", (0, 1, 37, 78, 79))

@@ -156,6 +156,19 @@ def test_flat_spectrum_k256_takes_the_single_a_buffer(kv, torch):
                   [(0, 0), (0, 1), (1, 0), (1, 1)], 1000)
 
 
+def test_cross_layer_pairs_k480_one_stage_projection(kv, torch):
+    """Cross-layer basis: two layers' rows side by side (D = 2048) under one
+    basis, 1 bit per coefficient.  The oracle's DP keeps k = 480 (30
+    groups) with 256-byte records: the projection runs two MMAs per K step
+    (N = 256 and 224) from a one-stage ring, the reconstruction contracts
+    k + 16 = 496 columns, the most its tensor memory holds."""
+    name, streams = "llama31_8b_8k_xlayer2", [(0, 0), (0, 1)]
+    blob = blob_for(name, calibrate_workload(name, streams))
+    assert {sc.basis.shape[1] for sc, _ in stream_calibs(blob).values()} \
+        == {480}
+    run_roundtrip(kv, torch, name, streams, 1000, ld_pad=64, blob=blob)
+
+
 def forced_blob(name, streams, ngroups, budget_bits):
     """Oracle basis of `name`'s streams with the first `ngroups` groups at
     width 1 and the rest dropped."""
