@@ -365,7 +365,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       mbar_init(&empty_b[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&a_full[i], 8);      // 4 prologue warps in each CTA
+      // the prologue warps that fill a buffer, in each CTA: one set of 4,
+      // or in a wide launch both sets (8), each with half of the groups
+      mbar_init(&a_full[i], kWide ? 16 : 8);
       mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < 4; ++i) {
@@ -584,10 +586,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
     for (int item = pair; item < total; item += npairs, ++it) {
       // A buffers: two of 128 columns, each filled by its own set of warps
       // on alternate tiles; or one of 256 columns (wide launch), filled by
-      // set 0 alone, tile after tile: with two sets on one buffer a set
-      // could wait on its barriers two phases ahead, where a parity wait
-      // cannot tell the phase it wants from the one before
-      if (kWide ? set != 0u : (it & 1u) != set) continue;
+      // both sets together tile after tile, each decoding half of the
+      // groups.  Both sets see every tile there, and a tile's buffer is
+      // released only after both sets' arrivals for the tile before, so
+      // neither set can wait on a barrier two phases ahead (where a parity
+      // wait cannot tell the phase it wants from the one before)
+      if (!kWide && (it & 1u) != set) continue;
       const uint32_t abuf = kWide ? 0u : it & 1u;
       const uint32_t ause = kWide ? it : it >> 1;
       const DecTile t = resolve(p, item);
@@ -747,7 +751,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       KVTC_TR(2)
       const uint32_t a_tmem =
           tmem + ((uint32_t)(q * 32) << 16) + 256u + abuf * 128u;
-      for (int a = 0; a < Ga; ++a) {
+      // groups [g0, g1) of this warp, and whether it writes the mean step
+      const int gh = (Ga + 1) >> 1;
+      const int g0 = kWide && set ? gh : 0, g1 = kWide && !set ? gh : Ga;
+      for (int a = g0; a < g1; ++a) {
         const int b = __shfl_sync(0xFFFFFFFFu, my_b, a);
         int po;
         uint32_t f;
@@ -799,7 +806,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         out[7] = dequant_pair(w3, 0x4342u, sc2, sh2);
         tmem_st8(a_tmem + (uint32_t)a * 8u, out);
       }
-      {
+      if (!kWide || set) {
         // the mean step: A = (1, 1, 0, ..., 0) against (mu_hi, mu_lo, 0...)
         const uint32_t ones[8] = {0x3C003C00u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
         tmem_st8(a_tmem + (uint32_t)Ga * 8u, ones);
