@@ -449,6 +449,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       // the next chunk's accumulator and B stage, when already known ready
       bool acc_ready = false, b_ready = false;
       const uint64_t desc_b0 = sw128_desc(smem_u32(sB));
+      // wide launch: the tile's first K-step slot of the cyclic A region
+      uint32_t slot0 = 0;
       for (int item = pair; item < total && ok; item += npairs) {
         const DecTile t = resolve(p, item);
         KVTC_TR(7)
@@ -462,9 +464,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         const int sstep = 4 * ds->kbs;       // K steps per B stage
         const int nbs = kWide ? ds->nbs : 1;
         const uint32_t idesc = make_idesc(256, (uint32_t)nc, 0);
-        // A buffers: two of 128 columns, or one of 256 (wide launch)
-        const uint32_t abuf = kWide ? 0u : it & 1u;
-        const uint32_t ause = kWide ? it : it >> 1;
+        // A buffers: two of 128 columns, or (wide launch) a cyclic region
+        // of 32 K-step slots of 8 columns where tiles take their ksteps
+        // slots one after another; the barriers alternate by tile
+        const uint32_t abuf = it & 1u;
+        const uint32_t ause = it >> 1;
         KVTC_TR(0)
         if (!mbar_wait(&a_full[abuf], ause & 1u, abort_flag)) {
           ok = false;
@@ -503,6 +507,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
             const int step0 = h * sstep;
             const int nsteps = min(ksteps - step0, sstep);
             const uint32_t a_h = a_col + (uint32_t)step0 * 8u;
+            const uint32_t sl_h = slot0 + (uint32_t)step0;
             // the next stage's and the next chunk's barriers are tested
             // (never waited on) right after the first MMA, so the test
             // overlaps the MMA run
@@ -510,7 +515,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
             const uint32_t ph_next = s + 1 == (uint32_t)nst ? ph ^ 1u : ph;
 #pragma unroll
             for (int step = 0; step < 4 * kDecMaxKbs; ++step) {
-              mma_ts_pair_if(d, a_h + (uint32_t)step * 8u,
+              mma_ts_pair_if(d,
+                             kWide ? tmem + 256u +
+                                         (((sl_h + (uint32_t)step) & 31u) << 3)
+                                   : a_h + (uint32_t)step * 8u,
                              bdesc + (uint64_t)((step >> 2) * kb_units +
                                                 (step & 3) * 2),
                              idesc, (h | step) > 0, step < nsteps);
@@ -536,6 +544,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         tc_commit_pair(&a_empty[abuf], 3);
         KVTC_TR(6)
         ++it;
+        slot0 = (slot0 + (uint32_t)ksteps) & 31u;
       }
       KVTC_TR(0)
       KVTC_TR_SAVE(0)
@@ -560,6 +569,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
     // each tile waits on memory once, for its records.
     int64_t nx_o0 = -1, nx_o1 = 0;
     uint32_t nx_hw = 0;
+    // wide launch: the tile's first slot of the cyclic A region (32 K-step
+    // slots of 8 columns, tiles taking Ga + 1 of them one after another)
+    // and the slot count of the tile before
+    uint32_t slot0 = 0;
+    int n_prev = 0;
     const auto pk_fetch = [&](int itm) {
       nx_o0 = -1;
       nx_o1 = 0;
@@ -585,15 +599,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
     KVTC_TR_DECL
     for (int item = pair; item < total; item += npairs, ++it) {
       // A buffers: two of 128 columns, each filled by its own set of warps
-      // on alternate tiles; or one of 256 columns (wide launch), filled by
-      // both sets together tile after tile, each decoding half of the
-      // groups.  Both sets see every tile there, and a tile's buffer is
-      // released only after both sets' arrivals for the tile before, so
-      // neither set can wait on a barrier two phases ahead (where a parity
-      // wait cannot tell the phase it wants from the one before)
+      // on alternate tiles; or (wide launch) a cyclic region of 256 columns
+      // filled by both sets together tile after tile, each decoding half of
+      // the groups.  Both sets see every tile there; a tile's slots are
+      // released by its MMAs (barriers alternating by tile, as for the two
+      // buffers), and a warp writes only after the release of the tile two
+      // back (and, for the slots it shares with it, of the tile before),
+      // so no wait is ever two phases ahead (where a parity wait cannot
+      // tell the phase it wants from the one before)
       if (!kWide && (it & 1u) != set) continue;
-      const uint32_t abuf = kWide ? 0u : it & 1u;
-      const uint32_t ause = kWide ? it : it >> 1;
+      const uint32_t abuf = it & 1u;
+      const uint32_t ause = it >> 1;
       const DecTile t = resolve(p, item);
       const DevStream* ds = p.streams + t.cs;
       const int R = ds->R, Ga = ds->Ga;
@@ -749,12 +765,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       KVTC_TR(1)
       __syncwarp();
       KVTC_TR(2)
-      const uint32_t a_tmem =
-          tmem + ((uint32_t)(q * 32) << 16) + 256u + abuf * 128u;
+      const uint32_t a_tmem = tmem + ((uint32_t)(q * 32) << 16) + 256u +
+                              (kWide ? 0u : abuf * 128u);
       // groups [g0, g1) of this warp, and whether it writes the mean step
       const int gh = (Ga + 1) >> 1;
       const int g0 = kWide && set ? gh : 0, g1 = kWide && !set ? gh : Ga;
+      // Wide launch: K step a of this tile lives in slot slot0 + a (mod 32).
+      // The wait above released the slots of the tile two back; the first
+      // 32 - n_prev steps miss the slots of the tile before, so they are
+      // written while its MMAs still run, and the others after its release.
+      const int conflict_from = it == 0u ? 32 : 32 - n_prev;
+      bool prev_free = false;
+      const auto a_col = [&](int a) -> uint32_t {
+        return kWide ? ((slot0 + (uint32_t)a) & 31u) << 3 : (uint32_t)a * 8u;
+      };
+      const auto claim = [&](int a) -> bool {
+        if (!kWide || prev_free || a < conflict_from) return true;
+        if (!mbar_wait(&a_empty[abuf ^ 1u], ((it - 1u) >> 1) & 1u,
+                       abort_flag))
+          return false;
+        tc_fence_after();
+        __syncwarp();
+        prev_free = true;
+        return true;
+      };
       for (int a = g0; a < g1; ++a) {
+        if (!claim(a)) {
+          ok = false;
+          break;
+        }
         const int b = __shfl_sync(0xFFFFFFFFu, my_b, a);
         int po;
         uint32_t f;
@@ -804,12 +843,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         out[5] = dequant_pair(w2, 0x4342u, sc2, sh2);
         out[6] = dequant_pair(w3, 0x4140u, sc2, sh2);
         out[7] = dequant_pair(w3, 0x4342u, sc2, sh2);
-        tmem_st8(a_tmem + (uint32_t)a * 8u, out);
+        tmem_st8(a_tmem + a_col(a), out);
       }
+      if (!ok) break;
       if (!kWide || set) {
         // the mean step: A = (1, 1, 0, ..., 0) against (mu_hi, mu_lo, 0...)
+        if (!claim(Ga)) {
+          ok = false;
+          break;
+        }
         const uint32_t ones[8] = {0x3C003C00u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-        tmem_st8(a_tmem + (uint32_t)Ga * 8u, ones);
+        tmem_st8(a_tmem + a_col(Ga), ones);
       }
       KVTC_TR(3)
       tmem_wait_st();
@@ -817,6 +861,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(a_full_leader + abuf * 8u);
       KVTC_TR(4)
+      if constexpr (kWide) {
+        slot0 = (slot0 + (uint32_t)(Ga + 1)) & 31u;
+        n_prev = Ga + 1;
+      }
     }
     KVTC_TR(0)
     KVTC_TR_SAVE(0)
