@@ -143,12 +143,12 @@ bool encode_blocked_3d(CUtensorMap* m, CUtensorMapDataType dt,
 // brings 128 rows of two consecutive 64-column K blocks, landing in shared
 // memory as two [128][64] tiles; 128-byte swizzle.
 bool encode_rows_kblocks(CUtensorMap* m, const void* base, uint64_t cols,
-                         uint64_t rows, uint64_t row_bytes) {
+                         uint64_t rows, uint64_t row_bytes, uint32_t kblocks) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {64, rows, cols / 64};
   cuuint64_t strides[2] = {row_bytes, 128};
-  cuuint32_t box[3] = {64u, (cuuint32_t)kTileM, 2u};
+  cuuint32_t box[3] = {64u, (cuuint32_t)kTileM, kblocks};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -762,7 +762,10 @@ int kvtc_calib_load(const void* blob, size_t blob_bytes, int cuda_device,
                            (uint32_t)(s.nc / 2), (uint32_t)s.kbs) ||
         !encode_blocked_3d(&s.tm_venc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                            dev + o.venc, (uint64_t)h.k, (uint64_t)(h.D / 64),
-                           (uint32_t)(h.k / 2), 2u)) {
+                           (uint32_t)(h.k / 2), 2u) ||
+        !encode_blocked_3d(&s.tm_venc1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                           dev + o.venc, (uint64_t)h.k, (uint64_t)(h.D / 64),
+                           (uint32_t)(h.k / 2), 1u)) {
       cudaFree(c->pool);
       delete c;
       return KVTC_ECUDA;
@@ -902,10 +905,23 @@ int kvtc_compress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
     const size_t i1 = std::min(cs.size(), i0 + kCompMaxSeg);
     int tiles = 0, kmax = 0, rmax = 0;
     for (size_t i = i0; i < i1; ++i) {
+      kmax = std::max(kmax, c->hs[cs[i]].k);
+      rmax = std::max(rmax, c->hs[cs[i]].R);
+    }
+    // A ring stage holds two K blocks (x tile and this CTA's V_enc half of
+    // each), or one where two such stages do not fit beside the record
+    // staging (k > 382 at 256-byte records); then the ring is as deep as
+    // fits
+    p->kps = 2;
+    if (compress_smem_bytes(2, 2 * (kTileM * 128 + kmax * 64), rmax / 4) >
+        232448)
+      p->kps = 1;
+    for (size_t i = i0; i < i1; ++i) {
       const HostStream& h = c->hs[cs[i]];
       CompSeg& g = p->seg[i - i0];
       if (!encode_rows_kblocks(&g.tm_x, src[slot[i]], (uint64_t)h.D,
-                               (uint64_t)(s_ + tc), 2ull * ld)) {
+                               (uint64_t)(s_ + tc), 2ull * ld,
+                               (uint32_t)p->kps)) {
         ret = KVTC_ECUDA;
         break;
       }
@@ -936,14 +952,11 @@ int kvtc_compress(const kvtc_calib* c, int layer0, int nlayers, int kv_mask,
     p->nseg = (int32_t)(i1 - i0);
     p->total_tiles = tiles;
     p->tiles_per_seg = (int32_t)((tc + kPairM - 1) / kPairM);
-    // a stage holds two K blocks: x [2][128][64] and this CTA's half of
-    // V_enc's k rows [2][k/2][64]
-    p->b_bytes_max = 2 * kmax * 64;
-    p->stage_bytes = 2 * kTileM * 128 + p->b_bytes_max;
+    // a stage holds kps K blocks: x [kps][128][64] and this CTA's half of
+    // V_enc's k rows [kps][k/2][64]
+    p->b_bytes_max = p->kps * kmax * 64;
+    p->stage_bytes = p->kps * kTileM * 128 + p->b_bytes_max;
     p->rec_stg_words = rmax / 4;
-    // the deepest ring that fits: two stages or more up to k = 382 at
-    // 256-byte records, one beyond (the load of the next K blocks then
-    // waits for the MMAs on this stage)
     int nst = 6;
     while (nst > 1 && compress_smem_bytes(nst, p->stage_bytes,
                                           p->rec_stg_words) > 232448)

@@ -28,6 +28,7 @@ struct DevStream {
                             // box {64, nc/2, kb}
   CUtensorMap tm_venc;      // bf16 V_kept, K-block major [D/64][k][64],
                             // box {64, k/2, 2}
+  CUtensorMap tm_venc1;     // the same, box {64, k/2, 1} (one K block)
   const float* mu;          // [D]   fp32 mean
   const float* m;           // [k]   fp32 projection of the mean
   const uint8_t* bits;      // [Ga]  width of each active group
@@ -92,7 +93,8 @@ struct CompParams {
   int32_t wide;             // a stream keeps k > 256: one k-column
                             // accumulator, two MMAs (N = 256, k - 256) per
                             // K step
-  int32_t pad2;
+  int32_t kps;              // K blocks per ring stage: 2, or 1 where two
+                            // stages of two do not fit
   RawList raw;              // sink/window rows and padding of these streams
 };
 

@@ -1122,12 +1122,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
         const DevStream* ds = p.streams + g.cs;
         const int nkb = ds->D / kAtomK;
         const int half = ds->k >> 1;
-        // a stage is two K blocks; both CTAs' x tiles and V_enc halves land
+        // a stage is kps K blocks; both CTAs' x tiles and V_enc halves land
         // on the leader's barrier (a box past the last K block is filled
         // with zeros and still counts its full bytes)
+        const int kps = p.kps;
         const uint32_t bytes_pair =
-            4u * ((uint32_t)kCompAStage + (uint32_t)half * 128u);
-        for (int kb = 0; kb < nkb; kb += 2) {
+            2u * (uint32_t)kps * ((uint32_t)kCompAStage + (uint32_t)half * 128u);
+        for (int kb = 0; kb < nkb; kb += kps) {
           KVTC_TR(0)
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) {
             ok = false;
@@ -1139,7 +1140,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
           tma_load_3d_pair(st, &g.tm_x, 0,
                            g.row0 + tile * kPairM + (int)rank * kTileM, kb,
                            full_leader + s * 8u);
-          tma_load_3d_pair(st + 2 * kCompAStage, &ds->tm_venc, 0,
+          tma_load_3d_pair(st + kps * kCompAStage,
+                           kps == 2 ? &ds->tm_venc : &ds->tm_venc1, 0,
                            (int)rank * half, kb, full_leader + s * 8u);
           ++it_b;
           if (++s == (uint32_t)nst) {
@@ -1170,7 +1172,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
       bool ok = true;
       const uint64_t desc_s0 = sw128_desc(smem_u32(smem));
       const uint64_t stage_units = (uint64_t)(stage_bytes >> 4);
-      const uint64_t b_units = (uint64_t)((2 * kCompAStage) >> 4);
+      const int kps = p.kps;
+      const uint64_t b_units = (uint64_t)((kps * kCompAStage) >> 4);
       const uint64_t a_kb_units = (uint64_t)(kCompAStage >> 4);
       for (int item = pair; item < total && ok; item += npairs) {
         const CompSeg& g = p.seg[find_comp_seg(p, item)];
@@ -1197,7 +1200,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
         tc_fence_after();
         KVTC_TR(1)
         const uint32_t d = tmem + accb * 256u;
-        for (int kb = 0; kb < nkb; kb += 2) {
+        for (int kb = 0; kb < nkb; kb += kps) {
           KVTC_TR(0)
           if (!mbar_wait(&full[s], ph, abort_flag)) {
             ok = false;
@@ -1205,11 +1208,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompThreads, 1)
           }
           tc_fence_after();
           KVTC_TR(2)
-          // two K blocks, four K=16 steps each: one unrolled run (the
-          // second block predicated off past the last K block)
+          // kps K blocks, four K=16 steps each: one unrolled run (a second
+          // block predicated off past the last K block, or in one-block
+          // stages)
           const uint64_t ad = desc_s0 + s * stage_units;
           const uint64_t bd = ad + b_units;
-          const uint32_t two = kb + 1 < nkb;
+          const uint32_t two = kps == 2 && kb + 1 < nkb;
           // (the tensor pipe queues almost nothing ahead, so a tile with
           // one MMA per K step runs without the second, predicated-off
           // instruction between its MMAs)
