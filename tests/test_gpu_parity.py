@@ -194,6 +194,50 @@ def test_hand_set_widths_k336_and_k448(kv, torch, ngroups, budget):
                       f"{16 * ngroups})")
 
 
+def mixed_blob(name, specs, budget_bits):
+    """Oracle bases of the streams in `specs` {(layer, kv): (groups, width)}
+    with that many leading groups at that width each (hand-set widths)."""
+    w = synth.WORKLOADS[name]
+    entries = []
+    for s, (ng, b) in specs.items():
+        widths = np.zeros(w.D // 16, dtype=np.int64)
+        widths[:ng] = b
+        entries += calibrate_forced(name, [s], widths)
+    return blob_for(name, entries, budget_bits)
+
+
+def test_mixed_k_in_one_launch(kv, torch):
+    """Six streams of one call keep k = 224, 336, 448, 496, 272 and 256
+    (hand-set widths, 256-byte records), 8192 tokens each: 192 super-tiles
+    over the CTA pairs, so a pair runs tiles of different streams one after
+    another.  The restore launch is wide: its cyclic A slots take tiles of
+    15 to 32 K steps back to back (a k = 496 tile fills all 32), each tile
+    waiting for the slots it shares with the one before.  The projection
+    runs one-K-block ring stages (k > 382 at 256-byte records) and two MMAs
+    per K step where k > 256."""
+    name = "llama31_8b_8k"
+    specs = {(2, 0): (14, 2), (2, 1): (21, 1), (3, 0): (28, 1),
+             (3, 1): (31, 1), (4, 0): (17, 2), (4, 1): (16, 2)}
+    blob = mixed_blob(name, specs, 2048)
+    assert sorted(sc.basis.shape[1] for sc, _ in
+                  stream_calibs(blob).values()) == [224, 256, 272, 336, 448,
+                                                    496]
+    run_roundtrip(kv, torch, name, list(specs), 8192, blob=blob,
+                  sample=lambda tc: np.arange(0, tc, 13),
+                  tag=f"{name}, k = 224 ... 496 in one launch")
+
+
+def test_paged_mixed_k(kv, torch):
+    """Paged restore of streams keeping k = 224 and k = 496 (256-byte
+    records) for five requests of different lengths: the wide paged kernel
+    with tiles of 15 and 32 K steps alternating through the cyclic A slots,
+    through the block table."""
+    name = "qwen25_7b_paged"
+    blob = mixed_blob(name, {(0, 0): (14, 2), (0, 1): (31, 1)}, 2048)
+    run_paged(kv, torch, name, [(0, 0), (0, 1)], [4096, 700, 4096, 300, 2000],
+              blob=blob, tag=f"{name}, k = 224 and 496")
+
+
 def test_paged_restore_k336(kv, torch):
     """Paged restore of the Qwen-shaped streams (D = 512, two output
     chunks) with 21 one-bit groups: k = 336 through the block table."""
