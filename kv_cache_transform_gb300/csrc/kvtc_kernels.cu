@@ -556,7 +556,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
   } else if (warp < 10) {
     // ------------------------------------ prologue: unpack + dequantise
     // Two sets of four warps (one per TMEM lane quadrant each): set 0 builds
-    // the A operand of the even super-tiles (buffer 0), set 1 of the odd.
+    // the A operand of the even super-tiles (buffer 0), set 1 of the odd;
+    // in a wide launch both sets build every tile's, half of its groups
+    // each.
     const int q = warp & 3;
     const uint32_t set = (uint32_t)(warp - 2) >> 2;
     uint32_t* stg = sRec + (warp - 2) * (rec_words * 33);
