@@ -801,8 +801,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
         uint32_t f;
         if constexpr (kPacked) {
           // packed record: the low bytes of the 2 Ga fields, the codes of
-          // their high bytes (per slot, v - vmin in d bits, then the high
-          // byte's low two bits), the bit-planes
+          // their high bytes (per slot, high byte - 4 vmin in d + 2 bits),
+          // the bit-planes
           po = __shfl_sync(0xFFFFFFFFu, pk_po, a);
           const uint32_t e = __shfl_sync(0xFFFFFFFFu, pk_grp, a);
           const uint32_t wi = min((e & 1023u) >> 5, (uint32_t)rec_words - 2u);
