@@ -270,6 +270,15 @@ def test_paged_restore_and_block_flag(kv, torch):
               [700, 37, 4096, 129])
 
 
+def test_paged_short_and_raw_only_requests(kv, torch):
+    """Requests shorter than a block, with no coded token (sink and window
+    only), of one token, with one coded token, and ending one token past a
+    256-token tile: sink and window rows exact, coded rows within the
+    restore tolerance, partial blocks written row by row."""
+    run_paged(kv, torch, "qwen25_7b_paged", [(0, 0), (0, 1)],
+              [3, 1, 16, 132, 133, 257, 389, 512])
+
+
 def test_paged_restore_256_byte_records(kv, torch):
     """Paged restore with the longest records (one-stage B ring)."""
     run_paged(kv, torch, "edge_d192_r256", [(0, 0), (0, 1)],
