@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -1035,7 +1036,7 @@ int kvtc_decompress_paged(const kvtc_calib* c, int layer0, int nlayers,
     for (int r0 = 0; r0 < R && ret == KVTC_OK; r0 += kPagedMaxReq) {
       const int r1 = std::min(R, r0 + kPagedMaxReq);
       std::memset(p, 0, sizeof(*p));
-      int tiles = 0;
+      int64_t tiles = 0;
       int64_t raw_chunks = 0;
       const int cpr = 2 * D / 16;
       for (int r = r0; r < r1; ++r) {
@@ -1047,14 +1048,20 @@ int kvtc_decompress_paged(const kvtc_calib* c, int layer0, int nlayers,
         p->tc[i] = (int32_t)tc;
         p->s_[i] = (int32_t)s_;
         p->raw_rows[i] = (int32_t)(s_ + w_);
-        p->tile_begin[i] = tiles;
+        p->tile_begin[i] = (int32_t)tiles;
         p->raw_begin[i] = raw_chunks;
         p->req_index[i] = r;
-        tiles += ns * paged_tiles((int)s_, (int)tc);
+        tiles += paged_tiles((int)s_, (int)tc);
         raw_chunks += (int64_t)ns * (s_ + w_) * cpr;
       }
-      p->tile_begin[r1 - r0] = tiles;
+      // stream-major: every stream of the launch has the same tiles
+      if (tiles * ns > INT32_MAX) {
+        ret = KVTC_ESIZE;
+        break;
+      }
+      p->tile_begin[r1 - r0] = (int32_t)tiles;
       p->raw_begin[r1 - r0] = raw_chunks;
+      tiles *= ns;
       int rmax = 0, kmax = 0;
       for (size_t j = j0; j < j1; ++j) {
         const int jl = (int)(j - j0);
@@ -1076,7 +1083,7 @@ int kvtc_decompress_paged(const kvtc_calib* c, int layer0, int nlayers,
       p->block_size = block_size;
       p->nreq = r1 - r0;
       p->nstream = ns;
-      p->total_tiles = tiles;
+      p->total_tiles = (int32_t)tiles;
       p->D = D;
       p->total_raw_chunks = raw_chunks;
       p->rec_words = rmax / 4;
@@ -1087,7 +1094,7 @@ int kvtc_decompress_paged(const kvtc_calib* c, int layer0, int nlayers,
           max_pairs_decompress(decompress_smem_bytes(p->nstages, p->rec_words));
       if (ret == KVTC_OK && tiles &&
           (mp < 1 ||
-           launch_decompress_paged(*p, pairs_for(mp, tiles), stream) !=
+           launch_decompress_paged(*p, pairs_for(mp, (int)tiles), stream) !=
                cudaSuccess))
         ret = KVTC_ECUDA;
     }

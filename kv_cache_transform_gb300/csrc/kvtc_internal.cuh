@@ -128,11 +128,12 @@ struct DecParams {
 static_assert(3 * kCompMaxSeg <= kRawListMax, "raw list too short");
 static_assert(2 * kDecMaxSeg <= kRawListMax, "raw list too short");
 
-// Paged restore: work items are (request, stream, tile).  A request's
-// tiles cover its tokens from token 0 (not from the first coded token), so
-// that each epilogue warp's 32 rows are two whole 16-token blocks; rows
-// without a record (sink, window, past the coded range) are decoded as
-// zeros and never stored.
+// Paged restore: work items are (stream, request, tile), stream-major, so
+// that the CTA pairs running side by side share one stream's basis.  A
+// request's tiles cover its tokens from token 0 (not from the first coded
+// token), so that each epilogue warp's 32 rows are two whole 16-token
+// blocks; rows without a record (sink, window, past the coded range) are
+// decoded as zeros and never stored.
 constexpr int kPagedMaxReq = 256;
 constexpr int kPagedMaxStream = 64;      // streams per launch
 // Super-tiles of one (request, stream): its tokens from 0 to the last one
@@ -148,7 +149,7 @@ struct PagedParams {
   int32_t tc[kPagedMaxReq];              // compressed tokens of request r
   int32_t s_[kPagedMaxReq];              // sink rows kept of request r
   int32_t raw_rows[kPagedMaxReq];        // s' + w' of request r
-  int32_t tile_begin[kPagedMaxReq + 1];
+  int32_t tile_begin[kPagedMaxReq + 1];  // request r's first tile in a stream
   int64_t raw_begin[kPagedMaxReq + 1];   // first raw 16-byte chunk of request r
   int32_t req_index[kPagedMaxReq];       // absolute request id (block table row)
   char* cache[kPagedMaxStream];          // pool of stream j

@@ -294,17 +294,17 @@ __device__ __forceinline__ DecTile resolve(const DecParams& p, int item) {
 }
 
 __device__ __forceinline__ DecTile resolve(const PagedParams& p, int item) {
+  const int per = max(1, p.tile_begin[p.nreq]);  // tiles of one stream
+  const int j = item / per;
+  const int idx = item - j * per;
   int lo = 0, hi = p.nreq - 1;
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
-    if (p.tile_begin[mid] <= item) lo = mid; else hi = mid - 1;
+    if (p.tile_begin[mid] <= idx) lo = mid; else hi = mid - 1;
   }
   const int r = lo;
-  const int tiles = max(1, paged_tiles(p.s_[r], p.tc[r]));
-  const int idx = item - p.tile_begin[r];
-  const int j = idx / tiles;
   DecTile t;
-  t.tile = idx - j * tiles;
+  t.tile = idx - p.tile_begin[r];
   t.cs = p.cs[j];
   t.tc = p.tc[r];
   t.rec = p.src[r] + (int64_t)p.sidx[j] * p.sbytes[r] +
