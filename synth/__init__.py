@@ -95,6 +95,12 @@ WORKLOADS = {
                           head_dim=128, tokens=900, requests=1, rank=384,
                           spectrum_p=0.0, outliers=False, sink=4, window=128,
                           avg_bits=2.5),
+    # the widest row the kernels take (D = 8192); 1024-bit budget, 128-byte
+    # records; signal rank 224
+    "edge_d8192": Workload("edge_d8192", layers=1, kv=(0, 1), heads=64,
+                           head_dim=128, tokens=600, requests=1, rank=224,
+                           spectrum_p=1.0, outliers=True, sink=4, window=16,
+                           avg_bits=0.125),
     "llama31_8b_8k": Workload("llama31_8b_8k", layers=32, kv=(0, 1), heads=8,
                               head_dim=128, tokens=8192, requests=1, rank=128,
                               spectrum_p=1.0, outliers=True, sink=4,

@@ -146,6 +146,36 @@ def test_d384_128_column_chunks(kv, torch):
                   900, ld_pad=64)
 
 
+def subspace_blob(name, streams, ngroups, width):
+    """Calibration built by hand for a row too wide for the oracle's PCA in
+    a test (D = 8192): the mean is the generator's, the basis an orthonormal
+    basis of the generator's signal subspace (QR of its mixing matrix), and
+    the first `ngroups` groups are kept at `width` bits."""
+    w = synth.WORKLOADS[name]
+    entries = []
+    for l, k in streams:
+        p = synth.stream_params(w, l, k)
+        q, _ = np.linalg.qr(p.A)
+        kk = 16 * ngroups
+        assert q.shape[1] >= kk
+        widths = np.zeros(w.D // 16, dtype=np.int64)
+        widths[:ngroups] = width
+        entries.append((l, k, p.mu, q[:, :kk], np.zeros(w.D), widths))
+    return blob_for(name, entries)
+
+
+def test_max_d8192(kv, torch):
+    """D = 8192, the widest row the kernels take: 128 K blocks per
+    projection tile and 32 output chunks per restore tile, contiguous and
+    paged (16-token blocks of 256 KB)."""
+    name, streams = "edge_d8192", [(0, 0), (0, 1)]
+    blob = subspace_blob(name, streams, 14, 2)
+    assert {sc.basis.shape for sc, _ in stream_calibs(blob).values()} == \
+        {(8192, 224)}
+    run_roundtrip(kv, torch, name, streams, 600, blob=blob)
+    run_paged(kv, torch, name, streams, [600, 37, 300], blob=blob)
+
+
 def test_flat_spectrum_k256_takes_the_single_a_buffer(kv, torch):
     """Flat spectrum at 1 bit per coefficient: the DP keeps 16 two-bit
     groups, k = 256.  The projection runs one N = 256 MMA per K step into
