@@ -1002,7 +1002,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDecThreads, 1)
           }
           if (any_rows) {
             // the other coded rows: 8 lanes per 128-byte row, four rows
-            // per store instruction
+            // per store instruction (unrolled by two only: fully unrolled,
+            // its live values push the kernel past its register cap)
+#pragma unroll 2
             for (int r0 = 0; r0 < 32; r0 += 4) {
               const int r = r0 + (lane >> 3);
               const int sub = lane & 7;
