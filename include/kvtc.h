@@ -29,6 +29,12 @@
  *     word, read and cleared with kvtc_device_status.
  *   - Pointers that the kernels reach with 16-byte vector or bulk copies
  *     must be 16-byte aligned, and row strides (ld) multiples of 8 elements.
+ *   - The calls are thread-safe on the host, and a launch's parameters
+ *     travel with the launch (nothing is staged in library-owned memory).
+ *     A loaded calibration is read-only on the device, so codec calls that
+ *     use it may run at the same time on several streams; their kernel
+ *     flags all land in its one status word.  The one exception is
+ *     kvtc_calib_mean_static (below).
  *
  * Formats (all little-endian):
  *
