@@ -309,6 +309,52 @@ def test_paged_short_and_raw_only_requests(kv, torch):
               [3, 1, 16, 132, 133, 257, 389, 512])
 
 
+def test_paged_host_refusals(kv, torch):
+    """What kvtc_decompress_paged refuses on the host, before any launch:
+    a block size other than 16, a block table too narrow for T, misaligned
+    stream, pool or block-table pointers, a negative T and an empty pool.
+    Nothing is written and no device flag is raised."""
+    name = "tiny"
+    w = synth.WORKLOADS[name]
+    calib = kv.kvtc_calib_load(blob_for(name, calibrate_workload(
+        name, [(0, 0)])), 0)
+    T, bs, maxb = 100, 16, 7
+    src = torch.zeros(calib.stream_bytes(0, 0, T), dtype=torch.uint8,
+                      device="cuda")
+    cache = torch.full((maxb + 1, bs, w.D), 0x7FC0, dtype=torch.int16,
+                       device="cuda")
+    bt = torch.arange(maxb, dtype=torch.int32, device="cuda").view(1, maxb)
+    good = dict(src=[src], T=[T], block_table=bt, max_blocks=maxb,
+                block_size=bs, cache=[cache], num_blocks=maxb + 1)
+
+    def refused(**change):
+        a = dict(good, **change)
+        with pytest.raises(kv.KvtcError) as e:
+            kv.kvtc_decompress_paged(calib, 0, 1, 1, a["src"], a["T"],
+                                     a["block_table"], a["max_blocks"],
+                                     a["block_size"], a["cache"],
+                                     a["num_blocks"])
+        return e.value.code
+
+    assert refused(block_size=8) == kv.KVTC_ENOTSUP
+    assert refused(max_blocks=maxb - 1, block_table=bt[:, :maxb - 1]
+                   .contiguous()) == kv.KVTC_ESIZE
+    assert refused(src=[src.data_ptr() + 8]) == kv.KVTC_EALIGN
+    assert refused(cache=[cache.data_ptr() + 2]) == kv.KVTC_EALIGN
+    assert refused(block_table=bt.data_ptr() + 2) == kv.KVTC_EALIGN
+    assert refused(T=[-1]) == kv.KVTC_EINVAL
+    assert refused(num_blocks=0) == kv.KVTC_EINVAL
+    torch.cuda.synchronize()
+    assert torch.all(cache == 0x7FC0)
+    assert kv.kvtc_device_status(calib) == 0
+    # the same arguments unchanged are accepted
+    kv.kvtc_decompress_paged(calib, 0, 1, 1, [src], [T], bt, maxb, bs,
+                             [cache], maxb + 1)
+    torch.cuda.synchronize()
+    assert kv.kvtc_device_status(calib) == 0
+    calib.free()
+
+
 def test_paged_restore_256_byte_records(kv, torch):
     """Paged restore with the longest records (one-stage B ring)."""
     run_paged(kv, torch, "edge_d192_r256", [(0, 0), (0, 1)],
