@@ -309,6 +309,61 @@ def test_paged_short_and_raw_only_requests(kv, torch):
               [3, 1, 16, 132, 133, 257, 389, 512])
 
 
+def test_codec_host_refusals(kv, torch):
+    """What kvtc_compress and kvtc_decompress refuse on the host, before any
+    launch: a row stride below D or off the 8-element grid, misaligned
+    pointers, an output or input buffer too small, a negative T, a layer
+    the calibration does not hold and an invalid K|V mask.  Nothing is
+    written and no device flag is raised; the same arguments unchanged are
+    accepted."""
+    name = "tiny"
+    w = synth.WORKLOADS[name]
+    calib = kv.kvtc_calib_load(blob_for(name, calibrate_workload(
+        name, [(0, 0)])), 0)
+    T, D = 300, w.D
+    x = to_dev(torch, synth.eval_tokens(w, 0, 0, T=T), D)
+    need = calib.stream_bytes(0, 0, T)
+    comp = torch.full((need + 64,), 0xA5, dtype=torch.uint8, device="cuda")
+    out = torch.full((T, D + 8), 0x7FC0, dtype=torch.int16, device="cuda")
+
+    def code(fn, *a):
+        with pytest.raises(kv.KvtcError) as e:
+            fn(calib, *a)
+        return e.value.code
+
+    c = kv.kvtc_compress
+    assert code(c, 0, 1, 1, [x], D - 8, T, comp, need) == kv.KVTC_ESIZE
+    assert code(c, 0, 1, 1, [x], D + 4, T, comp, need) == kv.KVTC_EALIGN
+    assert code(c, 0, 1, 1, [x.data_ptr() + 8], D, T, comp, need) == \
+        kv.KVTC_EALIGN
+    assert code(c, 0, 1, 1, [x], D, T, comp, need - 16) == kv.KVTC_ESIZE
+    assert code(c, 0, 1, 1, [x], D, T, comp.data_ptr() + 8, need) == \
+        kv.KVTC_EALIGN
+    assert code(c, 0, 1, 1, [x], D, -1, comp, need) == kv.KVTC_EINVAL
+    assert code(c, 5, 1, 1, [x], D, T, comp, need) == kv.KVTC_EINVAL
+    assert code(c, 0, 1, 0, [x], D, T, comp, need) == kv.KVTC_EINVAL
+    d = kv.kvtc_decompress
+    assert code(d, 0, 1, 1, comp, need, T, [out], D - 8) == kv.KVTC_ESIZE
+    assert code(d, 0, 1, 1, comp, need, T, [out], D + 4) == kv.KVTC_EALIGN
+    assert code(d, 0, 1, 1, comp, need, T, [out.data_ptr() + 8], D + 8) == \
+        kv.KVTC_EALIGN
+    assert code(d, 0, 1, 1, comp, need - 16, T, [out], D + 8) == \
+        kv.KVTC_ESIZE
+    assert code(d, 0, 1, 1, comp.data_ptr() + 8, need, T, [out], D + 8) == \
+        kv.KVTC_EALIGN
+    assert code(d, 0, 1, 1, comp, need, -1, [out], D + 8) == kv.KVTC_EINVAL
+    assert code(d, 0, 1, 4, comp, need, T, [out], D + 8) == kv.KVTC_EINVAL
+    torch.cuda.synchronize()
+    assert torch.all(comp == 0xA5) and torch.all(out == 0x7FC0)
+    assert kv.kvtc_device_status(calib) == 0
+    kv.kvtc_compress(calib, 0, 1, 1, [x], D, T, comp, need)
+    kv.kvtc_decompress(calib, 0, 1, 1, comp, need, T, [out], D + 8)
+    torch.cuda.synchronize()
+    assert kv.kvtc_device_status(calib) == 0
+    assert torch.all(comp[need:] == 0xA5) and torch.all(out[:, D:] == 0x7FC0)
+    calib.free()
+
+
 def test_paged_host_refusals(kv, torch):
     """What kvtc_decompress_paged refuses on the host, before any launch:
     a block size other than 16, a block table too narrow for T, misaligned
