@@ -238,3 +238,76 @@ def test_more_streams_than_one_launch_group(kv, torch):
     assert kv.kvtc_device_status(calib) == 0
     assert out.cpu().numpy().tobytes() == cb
     calib.free()
+
+
+def test_fields_host_refusals(kv, torch):
+    """What kvtc_fields_pack and kvtc_fields_unpack refuse on the host,
+    before any launch: buffers too small, misaligned pointers, a negative T
+    and an invalid K|V mask.  Nothing is written and no device flag is
+    raised; the same arguments unchanged then pack and unpack byte for
+    byte."""
+    name, T = "tiny", 300
+    w = synth.WORKLOADS[name]
+    blob, scs = workload_calib(name, [(0, 0)])
+    calib = kv.kvtc_calib_load(blob, 0)
+    comp = dev_bytes(torch, codec.compress_stream(
+        synth.eval_tokens(w, 0, 0, T=T), scs[(0, 0)][0]))
+    need = calib.stream_bytes(0, 0, T)
+    bound = kv.kvtc_fields_bound(calib, 0, 1, 1, T)
+    ws = kv.kvtc_fields_workspace_bytes(calib, 0, 1, 1)
+    assert ws >= 32
+    pk = torch.full((bound + 64,), 0xA5, dtype=torch.uint8, device="cuda")
+    offs = torch.full((4,), -7, dtype=torch.int64, device="cuda")
+    work = torch.zeros(ws + 64, dtype=torch.uint8, device="cuda")
+    back = torch.full((need + 64,), 0x5A, dtype=torch.uint8, device="cuda")
+    good = dict(src=comp, src_bytes=need, T=T, dst=pk, cap=bound,
+                offsets=offs, work=work, ws=ws, mask=1)
+
+    def pack_refused(**change):
+        a = dict(good, **change)
+        with pytest.raises(kv.KvtcError) as e:
+            kv.kvtc_fields_pack(calib, 0, 1, a["mask"], a["src"],
+                                a["src_bytes"], a["T"], a["dst"], a["cap"],
+                                a["offsets"], a["work"], a["ws"])
+        return e.value.code
+
+    assert pack_refused(src_bytes=need - 16) == kv.KVTC_ESIZE
+    assert pack_refused(cap=bound - 16) == kv.KVTC_ESIZE
+    assert pack_refused(ws=ws - 16) == kv.KVTC_ESIZE
+    assert pack_refused(src=comp.data_ptr() + 8) == kv.KVTC_EALIGN
+    assert pack_refused(dst=pk.data_ptr() + 8) == kv.KVTC_EALIGN
+    assert pack_refused(work=work.data_ptr() + 8) == kv.KVTC_EALIGN
+    assert pack_refused(offsets=offs.data_ptr() + 4) == kv.KVTC_EALIGN
+    assert pack_refused(T=-1) == kv.KVTC_EINVAL
+    assert pack_refused(mask=0) == kv.KVTC_EINVAL
+    torch.cuda.synchronize()
+    assert torch.all(pk == 0xA5) and torch.all(offs == -7)
+    assert kv.kvtc_device_status(calib) == 0
+    kv.kvtc_fields_pack(calib, 0, 1, 1, comp, need, T, pk, bound, offs, work,
+                        ws)
+    torch.cuda.synchronize()
+    size = int(offs[1].item())
+    assert int(offs[0].item()) == 0 and 256 <= size <= bound
+
+    def unpack_refused(src=pk, src_bytes=size, offsets=offs, T=T, dst=back,
+                       dst_bytes=need):
+        with pytest.raises(kv.KvtcError) as e:
+            kv.kvtc_fields_unpack(calib, 0, 1, 1, src, src_bytes, offsets, T,
+                                  dst, dst_bytes)
+        return e.value.code
+
+    assert unpack_refused(dst_bytes=need - 16) == kv.KVTC_ESIZE
+    assert unpack_refused(src_bytes=128) == kv.KVTC_ESIZE
+    assert unpack_refused(src=pk.data_ptr() + 8) == kv.KVTC_EALIGN
+    assert unpack_refused(dst=back.data_ptr() + 8) == kv.KVTC_EALIGN
+    assert unpack_refused(offsets=offs.data_ptr() + 4) == kv.KVTC_EALIGN
+    assert unpack_refused(T=-1) == kv.KVTC_EINVAL
+    torch.cuda.synchronize()
+    assert torch.all(back == 0x5A)
+    assert kv.kvtc_device_status(calib) == 0
+    kv.kvtc_fields_unpack(calib, 0, 1, 1, pk, size, offs, T, back, need)
+    torch.cuda.synchronize()
+    assert kv.kvtc_device_status(calib) == 0
+    assert torch.equal(back[:need], comp[:need])
+    assert torch.all(back[need:] == 0x5A)
+    calib.free()
