@@ -176,7 +176,9 @@ int kvtc_decompress(const kvtc_calib* calib, int layer0, int nlayers,
  *                  to block block_table[r*max_blocks + t/block_size], row
  *                  t % block_size.  Ids outside [0, num_blocks) are skipped
  *                  and flag KVTC_FLAG_BLOCK.
- *   block_size   : tokens per block (16).
+ *   block_size   : tokens per block; 16 (other sizes return ENOTSUP).
+ *   max_blocks   : columns of block_table; every request needs
+ *                  ceil(T[r] / block_size) of them (ESIZE otherwise).
  *   cache        : HOST array of 2*nlayers device pointers, each bf16
  *                  [num_blocks][block_size][D] (entries of kinds not in
  *                  kv_mask ignored).
